@@ -1,0 +1,67 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each case plants one mistake (a dropped term, a wrong sign or index, a
+transposed operand, a missing guard) in a temporary copy of ``kv_oracle.c``,
+builds it, and runs the pin suite against that copy: the suite must fail.
+Mistakes are planted on the CPU, in the oracle only.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from oracle.build import SOURCE, build_oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, original text, planted text)
+MUTANTS = [
+    ("coord_transposed", "return (layer * B + block) * T + token;",
+     "return (layer * T + block) * B + token;"),
+    ("coord_dropped_layer", "return (layer * B + block) * T + token;",
+     "return (block) * T + token;"),
+    ("paged_offset_wrong", "    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n"
+     "    return b * T + p % T;\n}\n\n/* [BT] Datenfluss",
+     "    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n"
+     "    return b * T + (p + 1) % T;\n}\n\n/* [BT] Datenfluss"),
+    ("paged_lb_off_by_one", "    int64_t lb = p / T;\n    if (lb >= stride)",
+     "    int64_t lb = p / T + 1;\n    if (lb >= stride)"),
+    ("paged_null_not_skipped", "    if (b == ORC_NULL_BLOCK) return ORC_PAD_SLOT;\n    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n    return b * T + p % T;\n}\n\n/* [BT]",
+     "    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n    return b * T + p % T;\n}\n\n/* [BT]"),
+    ("tail_not_padded", "for (int32_t t = 0; t < max_num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n        int32_t lo",
+     "for (int32_t t = 0; t < num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n        int32_t lo"),
+    ("range_sign", "int64_t b = (int64_t)rstart[i] + (lb - range_cum);",
+     "int64_t b = (int64_t)rstart[i] + (lb + range_cum);"),
+    ("range_cum_dropped", "            return b * T + p % T;\n        }\n        range_cum += len;",
+     "            return b * T + p % T;\n        }"),
+    ("range_bad_len_unflagged", "if (rlen[i] <= 0) return ORC_BAD_RANGE;", "if (rlen[i] < 0) return ORC_BAD_RANGE;"),
+    ("write_null_guard_dropped", "if (b == ORC_NULL_BLOCK) { *err |= ORC_NULL_WRITE; return -1; }", ""),
+    ("write_src_transposed", "int64_t src = ((int64_t)l * num_tokens + t) * E;",
+     "int64_t src = ((int64_t)t * num_layers + l) * E;"),
+    ("write_k_v_swapped", "k_cache[n * E + x] = key[src + x];", "k_cache[n * E + x] = value[src + x];"),
+    ("gather_offset_dropped", "o_r += s1 - s0;", "o_r += 0;"),
+    ("gather_v_from_k", "v_out[o * E + x] = n >= 0 ? v_cache[n * E + x] : 0;",
+     "v_out[o * E + x] = n >= 0 ? k_cache[n * E + x] : 0;"),
+    ("gather_token_offset", "src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);",
+     "src_rows[o] = orc_coord(layer, b, (p + 1) % block_size, num_blocks, block_size);"),
+    ("expand_formula", "out[c * k + j] = (int32_t)(m * k + j);", "out[c * k + j] = (int32_t)(m + j * k);"),
+    ("expand_null_expanded", "            if (m == ORC_NULL_BLOCK) continue;\n", ""),
+    ("expand_divisor_unchecked", "if (mgr_block_size % kernel_block_size != 0) return ORC_EUNSUPPORTED;", ""),
+]
+
+
+@pytest.mark.parametrize("name,orig,planted", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, orig, planted, tmp_path):
+    src = open(SOURCE).read()
+    assert src.count(orig) == 1, f"mutation anchor for {name} must occur exactly once"
+    mutant = tmp_path / "kv_oracle_mutant.c"
+    mutant.write_text(src.replace(orig, planted))
+    lib = build_oracle(extra_flags=["-Wno-unused-parameter", "-Wno-unused-variable",
+                                    "-Wno-unused-but-set-variable"],
+                       source=str(mutant), out=str(tmp_path / "libmutant.so"))
+    env = dict(os.environ, KV_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"planted mistake {name} went unnoticed:\n{r.stdout[-2000:]}"
