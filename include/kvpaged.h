@@ -1,0 +1,242 @@
+/*
+ * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
+ *
+ * Five calls, each one kernel launch on the caller's stream:
+ *   kv_slot_mapping_paged    token -> cache slot through a block table
+ *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
+ *   kv_cache_write           scatter new K/V rows into the paged caches
+ *   kv_cache_gather          gather a request's K/V through its block table
+ *   kv_expand_kernel_blocks  manager-size block table -> kernel-size blocks
+ *
+ * Sources (page title, section):
+ *   [BT]  "Blocktabelle" (vLLM v0.25.1 walkthrough)
+ *   [VBM] "vLLM Block Table Management" (PagedAttention, vLLM V1 block stack)
+ *   [RNG] "Range-addressed KV cache blocks for the vLLM serving engine"
+ *
+ * Common rules for every call
+ * ---------------------------
+ * Memory.  Every array argument is a device pointer owned by the caller
+ *   (for example a torch CUDA tensor).  The library allocates nothing, keeps
+ *   no state between calls and never synchronises: each call validates its
+ *   host-visible arguments, enqueues one kernel on `stream` and returns.
+ *   A pointer may be NULL only where the call reads nothing through it (for
+ *   example `positions` when num_tokens == 0).
+ * Layouts.  All arrays are dense, row-major, without padding between rows
+ *   other than the stated strides.  Block tables are int32
+ *   [rows, table_stride]: row r is request r, column j the physical block of
+ *   logical block j ([BT] Verantwortung).  Slot ids are int64, PAD = -1, and
+ *   block 0 is the null block ([VBM] Symbol Map; Deep Dive 8).  K and V are
+ *   separate bf16 caches [num_layers, num_blocks, block_size, num_kv_heads,
+ *   head_dim]; the row of (layer, block, token) is
+ *   n = (layer * num_blocks + block) * block_size + token and holds
+ *   num_kv_heads * head_dim contiguous elements ([RNG] The Coordinate
+ *   Approach).  All offsets are computed in 64 bits.
+ * Status.  The return value is a kv_status: KV_OK, or a negative code when a
+ *   host-visible argument is invalid (nothing is launched then), or
+ *   KV_ECUDA when the launch itself failed.
+ * Error word.  Data errors that only the device can see (a bad block id in a
+ *   table, a slot outside the cache, a malformed range row ...) never fault
+ *   and never stop the kernel: the affected token or row is skipped or
+ *   padded as documented per call, and the matching KV_ERR_* bit is OR-ed
+ *   into *d_err (int32, device memory, caller-cleared; d_err may be NULL to
+ *   ignore such errors).  Read it after the stream has reached the call.
+ * Empty work (zero tokens, zero requests) is valid and returns KV_OK.
+ */
+#ifndef KVPAGED_H
+#define KVPAGED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* kv_stream_t;
+
+enum kv_status {
+    KV_OK = 0,
+    KV_EINVAL = -1,        /* null/misaligned pointer, negative or inconsistent size */
+    KV_EUNSUPPORTED = -2,  /* a configuration the pages reject (fail closed) */
+    KV_ECUDA = -3          /* the kernel launch failed */
+};
+
+enum kv_error_bits {
+    KV_ERR_BAD_BLOCK = 1,     /* table/range block id outside [0, num_blocks) */
+    KV_ERR_BAD_SLOT = 2,      /* write slot at or past num_blocks * block_size */
+    KV_ERR_BAD_POSITION = 4,  /* negative position, or gather span invalid / past the table */
+    KV_ERR_BAD_RANGE = 8,     /* descriptor count outside [0, range_stride] or a range length <= 0 */
+    KV_ERR_NULL_WRITE = 16,   /* write slot inside the null block 0 */
+    KV_ERR_BAD_QSL = 32,      /* query_start_loc decreasing, negative, or past num_tokens */
+    KV_ERR_OUT_OF_SPACE = 64  /* gather output rows exceed out_rows */
+};
+
+#define KV_PAD_SLOT_ID (-1)
+#define KV_NULL_BLOCK_ID 0
+#define KV_MAX_RANGES_PER_REQ 256   /* [RNG] The Fork Implementation: capped at 256 ranges */
+#define KV_MAX_GATHER_REQS 4096     /* requests per kv_cache_gather call */
+
+/*
+ * kv_slot_mapping_paged -- per-token cache slot through the block table.
+ *
+ * Defined by [BT] Datenfluss (the slot-mapping kernel: block_index =
+ * pos // block_size, block_number = block_table[req, block_index],
+ * slot = block_number * block_size + pos % block_size; the last program pads
+ * [num_tokens, max_num_tokens) with PAD) and [VBM] Deep Dive 8.
+ *
+ *   query_start_loc  int32 [num_reqs + 1]; request r owns tokens
+ *                    [qsl[r], qsl[r+1]).  Must be non-decreasing.
+ *   positions        int64 [num_tokens]; position of each token in its request.
+ *   block_table      int32 [num_reqs, table_stride].
+ *   slot_mapping     int64 [max_num_tokens], written entirely.
+ *
+ * For token t < num_tokens of request r with position p:
+ *   p < 0                              -> PAD, KV_ERR_BAD_POSITION
+ *   p / block_size >= table_stride     -> PAD
+ *   b = block_table[r][p / block_size]:
+ *     b == 0 (null block)              -> PAD  ([BT] CUDA-Graph-Padding: null rows are skipped)
+ *     b < 0 or b >= num_blocks         -> PAD, KV_ERR_BAD_BLOCK
+ *     otherwise                        -> b * block_size + p % block_size
+ * Tokens in no request span, and tokens in [num_tokens, max_num_tokens), get
+ * PAD.  A decreasing qsl, qsl[0] < 0 or qsl[num_reqs] > num_tokens sets
+ * KV_ERR_BAD_QSL (slot values are then unspecified, but every store stays in
+ * bounds).
+ * Errors: KV_EINVAL for negative sizes, num_tokens > max_num_tokens,
+ * block_size <= 0, num_blocks < 1, table_stride < 0, or a null/misaligned
+ * pointer that would be read.
+ */
+int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64_t* positions,
+                          const int32_t* block_table, int32_t table_stride, int32_t num_reqs,
+                          int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
+                          int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
+                          kv_stream_t stream);
+
+/*
+ * kv_slot_mapping_range -- per-token cache slot through contiguous ranges.
+ *
+ * Defined by [RNG] The Innovation: physical_block = range_start +
+ * (pos // block_size - range_cum); positions outside every range get the
+ * same PAD id as the paged call.  The descriptor rows are loaded once per
+ * warp of 32 consecutive tokens of one request, never per position.
+ *
+ *   range_start, range_len  int32 [num_reqs, range_stride]; request r's ranges
+ *                           i < num_ranges[r] in logical order: range i holds
+ *                           logical blocks [cum_i, cum_i + range_len[r][i])
+ *                           with cum_i = sum of range_len[r][0..i-1], and
+ *                           logical block cum_i + j is physical block
+ *                           range_start[r][i] + j.
+ *   num_ranges              int32 [num_reqs].
+ *   other arguments         as kv_slot_mapping_paged.
+ *
+ * A logical block inside no range -> PAD.  The physical block b it resolves
+ * to is checked like a table entry (0 -> PAD; outside [0, num_blocks) -> PAD
+ * and KV_ERR_BAD_BLOCK).  A row with num_ranges[r] outside
+ * [0, range_stride] sets KV_ERR_BAD_RANGE and all its tokens get PAD; a
+ * range with length <= 0 sets KV_ERR_BAD_RANGE and covers no block.  Every
+ * row r < num_reqs is validated, with or without tokens.
+ * When block_table is the expansion of the ranges (and holds them all), the
+ * two calls return identical slot_mapping and error words ([RNG] Benchmark
+ * Methodology: both strategies produce identical slot ids).
+ * Errors: as kv_slot_mapping_paged; range_stride > KV_MAX_RANGES_PER_REQ is
+ * KV_EUNSUPPORTED ([RNG] The Fork Implementation: fail closed above 256).
+ */
+int kv_slot_mapping_range(const int32_t* query_start_loc, const int64_t* positions,
+                          const int32_t* range_start, const int32_t* range_len,
+                          const int32_t* num_ranges, int32_t range_stride, int32_t num_reqs,
+                          int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
+                          int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
+                          kv_stream_t stream);
+
+/*
+ * kv_cache_write -- scatter each new token's K and V rows to its slot.
+ *
+ * The cache write by slot of [BT] Verantwortung (kernels read and write KV
+ * directly through slot_mapping) and [VBM] Deep Dive 8; multi-layer
+ * addressing by [RNG] The Coordinate Approach.
+ *
+ *   key, value        bf16 [num_layers, num_tokens, num_kv_heads, head_dim].
+ *   k_cache, v_cache  bf16 [num_layers, num_blocks, block_size, num_kv_heads, head_dim].
+ *   slot_mapping      int64 [num_tokens].
+ *
+ * For every token t and layer l with s = slot_mapping[t]:
+ *   s < 0 (PAD)                 -> skipped
+ *   s / block_size == 0         -> skipped, KV_ERR_NULL_WRITE (block 0 is never written)
+ *   s >= num_blocks*block_size  -> skipped, KV_ERR_BAD_SLOT
+ *   otherwise cache row (l * num_blocks + s / block_size) * block_size + s % block_size
+ *   of k_cache (v_cache) receives key[l][t] (value[l][t]) bit for bit.
+ * Two tokens with the same slot race (one of the rows wins).
+ * Errors: KV_EINVAL for a null or non-16-byte-aligned K/V pointer, negative
+ * sizes, num_blocks < 1, block_size <= 0, num_kv_heads <= 0 or head_dim <= 0;
+ * KV_EUNSUPPORTED when num_kv_heads * head_dim * 2 is not a multiple of 16.
+ */
+int kv_cache_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                   const int64_t* slot_mapping, int32_t num_tokens, int32_t num_layers,
+                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t* d_err, kv_stream_t stream);
+
+/*
+ * kv_cache_gather -- read each request's K/V through its block table into
+ * contiguous buffers (the read-path resolution of [RNG] Block-table lookup
+ * per position; [VBM] Deep Dive 7: the kernel reads block_table[row][col]).
+ *
+ *   k_cache, v_cache  bf16 caches as in kv_cache_write; `layer` selects the layer.
+ *   block_table       int32 [num_reqs, table_stride].
+ *   gather_start/end  int32 [num_reqs]; request r asks for positions [start, end).
+ *   k_out, v_out      bf16 [out_rows, num_kv_heads, head_dim].
+ *
+ * Requests are packed in order: position p of request r goes to output row
+ * o_r + (p - start_r), o_r = sum of the earlier requests' lengths.  Each row:
+ *   table entry b = block_table[r][p / block_size]:
+ *     p / block_size >= table_stride -> zero row, KV_ERR_BAD_POSITION
+ *     b == 0 (null block)            -> zero row (padding and recycled blocks)
+ *     b < 0 or b >= num_blocks       -> zero row, KV_ERR_BAD_BLOCK
+ *     otherwise                      -> cache row (layer, b, p % block_size)
+ * A request with start < 0 or end < start contributes no rows and sets
+ * KV_ERR_BAD_POSITION.  Rows at or past out_rows are not written and set
+ * KV_ERR_OUT_OF_SPACE.  Output rows past the total are left untouched.
+ * Errors: KV_EINVAL as kv_cache_write, or layer outside [0, num_layers),
+ * out_rows < 0; KV_EUNSUPPORTED for a row size not a multiple of 16 bytes or
+ * num_reqs > KV_MAX_GATHER_REQS (split the batch).
+ */
+int kv_cache_gather(const void* k_cache, const void* v_cache, int32_t layer, int32_t num_layers,
+                    int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                    int32_t head_dim, const int32_t* block_table, int32_t table_stride,
+                    const int32_t* gather_start, const int32_t* gather_end, int32_t num_reqs,
+                    void* k_out, void* v_out, int64_t out_rows, int32_t* d_err,
+                    kv_stream_t stream);
+
+/*
+ * kv_expand_kernel_blocks -- unfold manager blocks into kernel blocks.
+ *
+ * [BT] Entwurfsmotivation (map_to_kernel_blocks unfolds one manager block
+ * into blocks_per_kv_block kernel blocks, e.g. manager 32 over kernel 16)
+ * and Grenzen und Fehler (a kernel block size that does not divide the
+ * manager block size is rejected).  With k = mgr_block_size /
+ * kernel_block_size, manager entry m at column c becomes kernel entries
+ * m*k + j at columns c*k + j, j < k; the null block 0 stays null (k zeros).
+ * Columns at or past mgr_stride * k are set to 0.  An entry m < 0, or one
+ * whose last kernel block would overflow int32, gives k null entries and
+ * KV_ERR_BAD_BLOCK.
+ *
+ *   mgr_table     int32 [num_reqs, mgr_stride].
+ *   kernel_table  int32 [num_reqs, kernel_stride], written entirely.
+ * Errors: KV_EUNSUPPORTED when mgr_block_size % kernel_block_size != 0;
+ * KV_EINVAL for block sizes <= 0, negative sizes, kernel_stride <
+ * mgr_stride * k, or null pointers with work to do.
+ */
+int kv_expand_kernel_blocks(const int32_t* mgr_table, int32_t num_reqs, int32_t mgr_stride,
+                            int32_t mgr_block_size, int32_t kernel_block_size,
+                            int32_t* kernel_table, int32_t kernel_stride, int32_t* d_err,
+                            kv_stream_t stream);
+
+/* Human-readable name of a kv_status value (static string). */
+const char* kv_status_string(int status);
+
+/* ABI version of this header (bumped on any signature change). */
+int kv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVPAGED_H */

@@ -1,0 +1,109 @@
+// kv_cache_write.cu -- scatter each new token's K and V rows into the paged
+// caches at its slot, for every layer.
+//
+// Sources: "Blocktabelle", Verantwortung (the attention kernels write KV
+// directly through slot_mapping); "vLLM Block Table Management", Deep Dive 8
+// (each token's KV is stored at exactly its slot); "Range-addressed KV cache
+// blocks ...", The Coordinate Approach (row n(layer, block, token) =
+// (layer * B + block) * T + token, offset n * bytes_per_token).
+//
+// GPU shape.  A row is num_kv_heads * head_dim bf16 values (2 KiB for 8x128),
+// contiguous in the input and in the cache, so one warp moves one (layer,
+// token) row pair with 16-byte vector accesses: 32 lanes x 16 B = 512 B per
+// instruction, fully coalesced on both sides.  Each lane keeps up to 4 K and
+// 4 V vectors in flight (4 KiB per warp).  The slot load and the K/V loads
+// are independent, so they are issued back to back and the DRAM round trips
+// overlap.  Warps walk the (layer, token) items in a grid-stride loop over a
+// persistent grid sized to the SM count, consecutive warps taking
+// consecutive tokens of one layer (contiguous input).  Everything is 64-bit
+// addressed: a 32-layer cache passes 2^32 bytes.
+#include "kv_common.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVecPerLane = 4;                 // 16-byte vectors per lane per chunk
+constexpr int kChunkVecs = 32 * kVecPerLane;   // 2 KiB per K (and V) chunk
+
+__global__ void __launch_bounds__(kThreads)
+cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                   uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                   const int64_t* __restrict__ slot_mapping, int32_t num_tokens,
+                   int64_t items, int64_t num_blocks, int32_t block_size, int32_t row_vecs,
+                   int32_t* err_word) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  uint32_t err = 0;
+  for (int64_t i = warp0; i < items; i += nwarps) {
+    const int64_t layer = i / num_tokens;
+    const int64_t t = i - layer * num_tokens;
+    const int64_t s = slot_mapping[t];
+    const uint4* ks = key + i * row_vecs;
+    const uint4* vs = value + i * row_vecs;
+    for (int c0 = 0; c0 < row_vecs; c0 += kChunkVecs) {
+      uint4 kr[kVecPerLane], vr[kVecPerLane];
+#pragma unroll
+      for (int j = 0; j < kVecPerLane; ++j) {
+        const int v = c0 + j * 32 + lane;
+        if (v < row_vecs) {
+          kr[j] = ld_stream(ks + v);
+          vr[j] = ld_stream(vs + v);
+        }
+      }
+      if (s < 0) break;  // PAD: nothing to store (warp-uniform)
+      const int64_t b = s / block_size;
+      if (b == kNull) { err |= KV_ERR_NULL_WRITE; break; }
+      if (b >= num_blocks) { err |= KV_ERR_BAD_SLOT; break; }
+      const int64_t n = (layer * num_blocks + b) * block_size + (s - b * block_size);
+      uint4* kd = k_cache + n * row_vecs;
+      uint4* vd = v_cache + n * row_vecs;
+#pragma unroll
+      for (int j = 0; j < kVecPerLane; ++j) {
+        const int v = c0 + j * 32 + lane;
+        if (v < row_vecs) {
+          kd[v] = kr[j];
+          vd[v] = vr[j];
+        }
+      }
+    }
+  }
+  report(err_word, err);
+}
+
+}  // namespace
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" int kv_cache_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                              const int64_t* slot_mapping, int32_t num_tokens,
+                              int32_t num_layers, int64_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t* d_err,
+                              kv_stream_t stream) {
+  if (num_tokens < 0 || num_layers < 0 || num_blocks < 1 || block_size <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0)
+    return KV_EINVAL;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
+  if (row_bytes % 16 != 0 || row_bytes / 16 > INT32_MAX) return KV_EUNSUPPORTED;
+  if (d_err != nullptr && !aligned(d_err, 4)) return KV_EINVAL;
+  const int64_t items = (int64_t)num_layers * num_tokens;
+  if (items == 0) return KV_OK;
+  if (key == nullptr || value == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      slot_mapping == nullptr)
+    return KV_EINVAL;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+    return KV_EINVAL;
+  const int32_t row_vecs = (int32_t)(row_bytes / 16);
+  const int64_t warps_needed = items;
+  const int64_t ctas_needed = (warps_needed * 32 + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)sm_count() * (2048 / kThreads);
+  const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);
+  cache_write_kernel<<<grid, kThreads, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
+      items, num_blocks, block_size, row_vecs, d_err);
+  return launch_status();
+}

@@ -1,0 +1,110 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects invalid host-visible arguments before launching
+anything (these calls never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvpaged.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_39_gb300 import _lib
+    from paged_kv_cache_39_gb300 import build as kbuild
+    if not os.path.exists(_lib.LIB_PATH):
+        kbuild.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(kv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for fn in ["kv_slot_mapping_paged", "kv_slot_mapping_range", "kv_cache_write",
+               "kv_cache_gather", "kv_expand_kernel_blocks"]:
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from paged_kv_cache_39_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kv_abi_version() == 1
+    assert lib.kv_status_string(0) == b"KV_OK"
+    assert b"EINVAL" in lib.kv_status_string(-1)
+    assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
+
+
+N = None
+
+
+def test_slot_mapping_rejects_bad_arguments(lib):
+    # negative sizes, num_tokens > max_num_tokens, block_size <= 0, missing pointers
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, -1, 0, 0, 16, 8, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, 0, 5, 4, 16, 8, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, 0, 0, 0, 0, 8, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, 0, 0, 0, 16, 0, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, 1, 0, 0, 16, 8, N, N, N) == -1  # qsl NULL
+    assert lib.kv_slot_mapping_paged(N, N, N, 0, 0, 0, 4, 16, 8, N, N, N) == -1  # slots NULL
+    # misaligned positions pointer
+    assert lib.kv_slot_mapping_paged(N, 0x1004, N, 0, 0, 1, 1, 16, 8, 0x2000, N, N) == -1
+
+
+def test_range_cap_fails_closed(lib):
+    assert lib.kv_slot_mapping_range(N, N, N, N, N, 257, 0, 0, 0, 16, 8, N, N, N) == -2
+    assert lib.kv_slot_mapping_range(N, N, N, N, N, -1, 0, 0, 0, 16, 8, N, N, N) == -1
+
+
+def test_write_rejects_bad_arguments(lib):
+    # row of 8x7 bf16 = 112 B is a multiple of 16: OK shape; 3x5 = 30 B is not
+    assert lib.kv_cache_write(N, N, N, N, N, 1, 1, 8, 16, 3, 5, N, N) == -2
+    assert lib.kv_cache_write(N, N, N, N, N, 1, 1, 8, 16, 8, 64, N, N) == -1  # NULL K/V
+    assert lib.kv_cache_write(0x1008, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 8, 16, 8, 64, N,
+                              N) == -1  # key not 16-byte aligned
+    assert lib.kv_cache_write(N, N, N, N, N, 1, 1, 0, 16, 8, 64, N, N) == -1
+    assert lib.kv_cache_write(N, N, N, N, N, 0, 1, 8, 16, 8, 64, N, N) == 0  # nothing to do
+
+
+def test_gather_rejects_bad_arguments(lib):
+    args = dict(kc=0x1000, vc=0x2000)
+    assert lib.kv_cache_gather(args["kc"], args["vc"], 1, 1, 8, 16, 8, 64, N, 0, N, N, 0, N, N,
+                               0, N, N) == -1  # layer out of range
+    assert lib.kv_cache_gather(args["kc"], args["vc"], 0, 1, 8, 16, 8, 64, N, 0, N, N, 4097, N,
+                               N, 0, N, N) == -2  # too many requests
+    assert lib.kv_cache_gather(args["kc"], args["vc"], 0, 1, 8, 16, 8, 64, N, 0, N, N, 0, N, N,
+                               0, N, N) == 0  # no requests
+    assert lib.kv_cache_gather(args["kc"], args["vc"], 0, 1, 8, 16, 8, 64, N, 4, 0x3000, 0x4000,
+                               2, N, N, 8, N, N) == -1  # table NULL with stride > 0
+
+
+def test_expand_rejects_bad_arguments(lib):
+    assert lib.kv_expand_kernel_blocks(N, 1, 4, 32, 12, N, 16, N, N) == -2  # non-divisor
+    assert lib.kv_expand_kernel_blocks(N, 1, 4, 16, 32, N, 16, N, N) == -2
+    assert lib.kv_expand_kernel_blocks(N, 1, 4, 32, 16, N, 7, N, N) == -1  # stride too small
+    assert lib.kv_expand_kernel_blocks(N, 1, 4, 0, 16, N, 8, N, N) == -1
+    assert lib.kv_expand_kernel_blocks(N, 0, 4, 32, 16, N, 8, N, N) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import paged_kv_cache_39_gb300 as kv
+    q = torch.zeros(2, dtype=torch.int32)
+    p = torch.zeros(1, dtype=torch.int64)
+    t = torch.zeros((1, 8), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kv.kv_slot_mapping_paged(q, p, t, 16, 8)
+    kc = torch.zeros((1, 4, 16, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kv.kv_cache_gather(kc, kc, t, q[:1], q[:1])

@@ -1,0 +1,227 @@
+"""GPU parity at the workloads' full sizes, in the launch configurations the
+benchmark times.
+
+Slot maps and expanded tables are compared whole with the oracle.  For the
+KV copies, the oracle computes the destination (write) or source (gather)
+row of every output row; every row is then checked on the device (torch only
+moves the bytes being compared) and a random sample of rows is checked on
+the host against cache rows fetched one by one.  Caches that the write does
+not address must keep their fill pattern, the null block included.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_39_gb300 as kv
+from paged_kv_cache_39_gb300 import workloads as wl
+from gpu_helpers import (bits, cuda, dev, device_rows_equal, err_word, free_bytes, rows_view,
+                         sample_host_check)
+
+pytestmark = pytest.mark.gpu
+
+FILL = 0x3C01  # bf16 bit pattern of the caches before the write (1.0078125)
+SAMPLE = 2048
+
+
+@pytest.fixture(autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kv.load()
+    torch.cuda.set_device(dev())
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def filled_cache(shape):
+    return torch.full(shape, FILL, dtype=torch.int16, device=dev()).view(torch.bfloat16)
+
+
+def slot_maps_match(w, lay, check_range=True):
+    T, B = w.block_size, w.num_blocks
+    exp, exp_e = oracle.slot_mapping_paged(w.qsl, w.positions, lay.table, w.num_tokens,
+                                           w.max_num_tokens, T, B)
+    qsl, pos = cuda(w.qsl), cuda(w.positions)
+    e = err_word()
+    sp = kv.kv_slot_mapping_paged(qsl, pos, cuda(lay.table), T, B,
+                                  max_num_tokens=w.max_num_tokens, err=e)
+    assert int(e.item()) == exp_e == 0
+    assert np.array_equal(sp.cpu().numpy(), exp)
+    if check_range and lay.range_start is not None:
+        exp_r, exp_re = oracle.slot_mapping_range(w.qsl, w.positions, lay.range_start,
+                                                  lay.range_len, lay.num_ranges, w.num_tokens,
+                                                  w.max_num_tokens, T, B)
+        e = err_word()
+        sr = kv.kv_slot_mapping_range(qsl, pos, cuda(lay.range_start), cuda(lay.range_len),
+                                      cuda(lay.num_ranges), T, B,
+                                      max_num_tokens=w.max_num_tokens, err=e)
+        assert int(e.item()) == exp_re == 0
+        assert np.array_equal(sr.cpu().numpy(), exp_r)
+        assert np.array_equal(exp_r, exp)  # range == paged slot for slot
+    return sp, exp
+
+
+def check_write(key, val, kc, vc, slots_host, L, N, B, T, E, rng):
+    """Oracle destination rows; full device check; sampled host check; untouched rows."""
+    dest, exp_e = oracle.write_rows(slots_host, N, L, B, T)
+    flat_dest = dest.reshape(-1)
+    valid = np.nonzero(flat_dest >= 0)[0]
+    # every written row holds its token's K/V row
+    src_k = rows_view(key, E)
+    src_v = rows_view(val, E)
+    kr, vr = rows_view(kc, E), rows_view(vc, E)
+    for s in range(0, len(valid), 1 << 16):
+        sel = torch.from_numpy(valid[s:s + (1 << 16)]).to(dev())
+        drow = torch.from_numpy(flat_dest[valid[s:s + (1 << 16)]]).to(dev())
+        assert torch.equal(kr.index_select(0, drow), src_k.index_select(0, sel))
+        assert torch.equal(vr.index_select(0, drow), src_v.index_select(0, sel))
+    # sampled host check through the oracle's per-row arithmetic
+    pick = rng.choice(len(valid), size=min(SAMPLE, len(valid)), replace=False)
+    for i in valid[pick][:256]:
+        l, t = divmod(int(i), N)
+        got = kr[int(flat_dest[i])].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, src_k[l * N + t].cpu().numpy().view(np.uint16))
+    # nothing else changed: rows differing from the fill pattern are exactly the written ones
+    fill64 = torch.tensor([FILL], dtype=torch.int16).repeat(4).view(torch.int64).item()
+    changed = 0
+    for c in (kc, vc):
+        per_layer = c.view(L, -1)
+        for l in range(L):
+            v64 = per_layer[l].view(torch.int16).view(-1, E).view(torch.int64)
+            changed += int((v64 != fill64).any(dim=1).sum().item())
+    assert changed == 2 * len(np.unique(flat_dest[valid]))
+    return exp_e
+
+
+def test_decode_full():
+    w = wl.decode()
+    lay = w.layouts["G"]
+    T, B, H, D, E = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim, w.row_elems
+    sp, exp = slot_maps_match(w, lay)
+    key = wl.bf16_normal((1, w.num_tokens, H, D), 101, dev())
+    val = wl.bf16_normal((1, w.num_tokens, H, D), 102, dev())
+    kc, vc = filled_cache((1, B, T, H, D)), filled_cache((1, B, T, H, D))
+    e = err_word()
+    kv.kv_cache_write(key, val, kc, vc, sp, err=e)
+    exp_e = check_write(key, val, kc, vc, exp, 1, w.num_tokens, B, T, E,
+                        np.random.default_rng(1))
+    assert int(e.item()) == exp_e == 0
+    # the decode batch's contexts read back through the table: the new token
+    # is the last row of each request's span
+    rows = int(w.gather_end.sum())
+    e = err_word()
+    k_out, v_out = kv.kv_cache_gather(kc, vc, cuda(lay.table), cuda(w.gather_start),
+                                      cuda(w.gather_end), out_rows=rows, err=e)
+    src, exp_ge = oracle.gather_rows(0, B, T, lay.table, w.gather_start, w.gather_end, rows)
+    assert int(e.item()) == exp_ge == 0
+    assert device_rows_equal(k_out, kc, src, E) and device_rows_equal(v_out, vc, src, E)
+    last = np.cumsum(w.gather_end.astype(np.int64)) - 1
+    assert torch.equal(rows_view(k_out, E)[torch.from_numpy(last).to(dev())], rows_view(key[0], E))
+
+
+def test_mixed_full():
+    need = 2 * 32 * 49152 * 16 * 2048 + (8 << 30)
+    if free_bytes() >= need:
+        w = wl.mixed()
+    else:  # reduced pool, recorded in the test output
+        print("mixed: reduced to 32768 blocks / decode ctx U{512..2048} for free memory")
+        w = wl.mixed(num_blocks=32768, decode_ctx_max=2048)
+    lay = w.layouts["G"]
+    T, B, L, H, D, E = (w.block_size, w.num_blocks, w.num_layers, w.num_kv_heads, w.head_dim,
+                        w.row_elems)
+    sp, exp = slot_maps_match(w, lay)
+    key = wl.bf16_normal((L, w.num_tokens, H, D), 201, dev())
+    val = wl.bf16_normal((L, w.num_tokens, H, D), 202, dev())
+    kc, vc = filled_cache((L, B, T, H, D)), filled_cache((L, B, T, H, D))
+    e = err_word()
+    kv.kv_cache_write(key, val, kc, vc, sp, err=e)
+    exp_e = check_write(key, val, kc, vc, exp, L, w.num_tokens, B, T, E, np.random.default_rng(2))
+    assert int(e.item()) == exp_e == 0
+    # null block 0 of every layer is untouched
+    assert (kc.view(torch.int16)[:, 0] == FILL).all() and (vc.view(torch.int16)[:, 0] == FILL).all()
+
+
+@pytest.mark.parametrize("layout", ["P", "G"])
+def test_long_context_full(layout):
+    w = wl.long_context()
+    lay = w.layouts[layout]
+    T, B, H, D, E = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim, w.row_elems
+    slot_maps_match(w, lay)
+    kc = wl.bf16_normal((1, B, T, H, D), 301, dev())
+    vc = wl.bf16_normal((1, B, T, H, D), 302, dev())
+    rows = w.num_tokens
+    e = err_word()
+    k_out, v_out = kv.kv_cache_gather(kc, vc, cuda(lay.table), cuda(w.gather_start),
+                                      cuda(w.gather_end), out_rows=rows, err=e)
+    src, exp_e = oracle.gather_rows(0, B, T, lay.table, w.gather_start, w.gather_end, rows)
+    assert int(e.item()) == exp_e == 0
+    assert device_rows_equal(k_out, kc, src, E) and device_rows_equal(v_out, vc, src, E)
+    rng = np.random.default_rng(3)
+    sample = np.sort(rng.choice(rows, size=SAMPLE, replace=False))
+    kflat = rows_view(kc, E)
+    sample_host_check(k_out, lambda n: kflat[n].cpu().numpy().view(np.uint16), src, E, sample)
+    if layout == "G":
+        # one packed run per range: the first range of request 0 is one contiguous copy
+        s0, ln0 = int(lay.range_start[0, 0]), int(lay.range_len[0, 0])
+        assert torch.equal(rows_view(k_out, E)[:ln0 * T], kflat[s0 * T:(s0 + ln0) * T])
+
+
+def test_hybrid_full():
+    h = wl.hybrid()
+    H, D, E = h.num_kv_heads, h.head_dim, h.num_kv_heads * h.head_dim
+    qsl, pos = cuda(h.qsl), cuda(h.positions)
+    rng = np.random.default_rng(4)
+    key = wl.bf16_normal((1, h.num_tokens, H, D), 401, dev())
+    val = wl.bf16_normal((1, h.num_tokens, H, D), 402, dev())
+    for name, g in h.groups.items():
+        kbs = g.kernel_block_size
+        Bk = g.kernel_num_blocks
+        # 32 -> 16 expansion of the manager table
+        exp_kt, exp_xe = oracle.expand_kernel_blocks(g.mgr_table, g.mgr_block_size, kbs)
+        e = err_word()
+        kt = kv.kv_expand_kernel_blocks(cuda(g.mgr_table), g.mgr_block_size, kbs, err=e)
+        assert int(e.item()) == exp_xe == 0
+        assert np.array_equal(kt.cpu().numpy(), exp_kt)
+        # decode slot map over the kernel table, padded rows and tail PAD
+        exp_s, exp_se = oracle.slot_mapping_paged(h.qsl, h.positions, exp_kt, h.num_tokens,
+                                                  h.max_num_tokens, kbs, Bk)
+        e = err_word()
+        sp = kv.kv_slot_mapping_paged(qsl, pos, kt, kbs, Bk, max_num_tokens=h.max_num_tokens,
+                                      err=e)
+        assert int(e.item()) == exp_se == 0
+        assert np.array_equal(sp.cpu().numpy(), exp_s)
+        assert (exp_s[h.num_tokens:] == -1).all()
+        # decode write of one token per real request
+        kc = wl.bf16_normal((1, Bk, kbs, H, D), 410 + len(name), dev())
+        vc = wl.bf16_normal((1, Bk, kbs, H, D), 420 + len(name), dev())
+        dest, exp_we = oracle.write_rows(exp_s[:h.num_tokens], h.num_tokens, 1, Bk, kbs)
+        e = err_word()
+        kv.kv_cache_write(key, val, kc, vc, sp[:h.num_tokens], err=e)
+        assert int(e.item()) == exp_we == 0
+        drow = torch.from_numpy(dest[0]).to(dev())
+        assert torch.equal(rows_view(kc, E)[drow], rows_view(key, E))
+        assert torch.equal(rows_view(vc, E)[drow], rows_view(val, E))
+        # gather: 8 calls of 64 requests, then the 128 padding rows (no rows, no error)
+        kflat = rows_view(kc, E)
+        for c in range(0, h.num_reqs, 64):
+            hi = min(h.num_reqs, c + 64) if c < h.num_real_reqs else h.num_reqs
+            g0, g1 = g.gather_start[c:hi], g.gather_end[c:hi]
+            rows = int((g1.astype(np.int64) - g0).sum())
+            e = err_word()
+            k_out, v_out = kv.kv_cache_gather(kc, vc, kt[c:hi].contiguous(), cuda(g0), cuda(g1),
+                                              out_rows=rows, err=e)
+            src, exp_ge = oracle.gather_rows(0, Bk, kbs, exp_kt[c:hi], g0, g1, rows)
+            assert int(e.item()) == exp_ge == 0
+            if rows:
+                assert device_rows_equal(k_out, kc, src, E)
+                assert device_rows_equal(v_out, vc, src, E)
+                sample = np.sort(rng.choice(rows, size=min(256, rows), replace=False))
+                sample_host_check(v_out, lambda n: rows_view(vc, E)[n].cpu().numpy().view(np.uint16),
+                                  src, E, sample)
+                assert (src >= 0).all()  # SWA windows never touch recycled blocks
+            if c >= h.num_real_reqs:
+                assert rows == 0
+                break
+        del kc, vc, kt, kflat
+        torch.cuda.empty_cache()

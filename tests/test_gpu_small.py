@@ -1,0 +1,349 @@
+"""GPU parity on small and adversarial cases: every output of every kernel is
+compared element by element with the CPU oracle (bit-exact, tolerance 0:
+outputs are integers or copied bf16 bits), together with the error word."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_39_gb300 as kv
+from paged_kv_cache_39_gb300 import workloads as wl
+from gpu_helpers import bits, cuda, dev, err_word
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kv.load()  # fails loudly when the CUDA library is missing
+    torch.cuda.set_device(dev())
+    yield
+    torch.cuda.synchronize()
+
+
+def run_paged(qsl, pos, table, N, n_max, T, B):
+    e = err_word()
+    s = kv.kv_slot_mapping_paged(cuda(np.asarray(qsl, np.int32)), cuda(np.asarray(pos, np.int64)),
+                                 cuda(np.asarray(table, np.int32)), T, B, max_num_tokens=n_max,
+                                 num_tokens=N, err=e)
+    return s.cpu().numpy(), int(e.item())
+
+
+def run_range(qsl, pos, rs, rl, nr, N, n_max, T, B):
+    e = err_word()
+    s = kv.kv_slot_mapping_range(cuda(np.asarray(qsl, np.int32)), cuda(np.asarray(pos, np.int64)),
+                                 cuda(np.asarray(rs, np.int32)), cuda(np.asarray(rl, np.int32)),
+                                 cuda(np.asarray(nr, np.int32)), T, B, max_num_tokens=n_max,
+                                 num_tokens=N, err=e)
+    return s.cpu().numpy(), int(e.item())
+
+
+# ------------------------------------------------------------------ golden
+
+
+def test_figure6_on_gpu(golden):
+    g = golden("figure6_bs4.json")
+    T = g["block_size"]
+    for step in g["steps"]:
+        row = np.zeros((1, 8), np.int32)
+        row[0, :len(step["row"])] = step["row"]
+        n = len(step["positions"])
+        s, e = run_paged([0, n], step["positions"], row, n, n, T, 16)
+        assert e == 0 and s.tolist() == step["slots"]
+    rs = np.zeros((1, 256), np.int32)
+    rl = np.zeros((1, 256), np.int32)
+    for i, (a, b) in enumerate(g["ranges_final_row"]):
+        rs[0, i], rl[0, i] = a, b
+    pos = sum((st["positions"] for st in g["steps"]), [])
+    s, e = run_range([0, len(pos)], pos, rs, rl, [3], len(pos), len(pos), T, 16)
+    assert e == 0 and s.tolist() == sum((st["slots"] for st in g["steps"]), [])
+
+
+def test_page3_on_gpu(golden):
+    g = golden("page3_bs16.json")
+    row = np.zeros((1, 8), np.int32)
+    row[0, :2] = g["row"]
+    n = len(g["positions"])
+    s, e = run_paged([0, n], g["positions"], row, n, n + 3, g["block_size"], 16)
+    assert e == 0
+    assert s[:16].tolist() == list(range(112, 128)) and s[16] == 16 and (s[n:] == -1).all()
+
+
+def test_expand_golden_on_gpu(golden):
+    g = golden("expand_32_16.json")
+    e = err_word()
+    out = kv.kv_expand_kernel_blocks(cuda(np.array([g["mgr_row"]], np.int32)),
+                                     g["mgr_block_size"], g["kernel_block_size"], err=e)
+    assert out.cpu().numpy()[0].tolist() == g["kernel_row"] and int(e.item()) == 0
+    for mbs, kbs in g["rejected"]:
+        with pytest.raises(kv.KVError) as ei:
+            kv.kv_expand_kernel_blocks(cuda(np.array([[1]], np.int32)), mbs, kbs,
+                                       kernel_table=torch.empty((1, 4), dtype=torch.int32,
+                                                                device=dev()))
+        assert ei.value.status == kv.KV_EUNSUPPORTED
+
+
+# -------------------------------------------------------------- tiny config
+
+
+@pytest.mark.parametrize("layout", ["P", "G"])
+def test_tiny_whole_path(layout):
+    w = wl.tiny()
+    lay = w.layouts[layout]
+    T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
+    exp_s, exp_e = oracle.slot_mapping_paged(w.qsl, w.positions, lay.table, w.num_tokens,
+                                             w.max_num_tokens, T, B)
+    s, e = run_paged(w.qsl, w.positions, lay.table, w.num_tokens, w.max_num_tokens, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    s2, e2 = run_range(w.qsl, w.positions, lay.range_start, lay.range_len, lay.num_ranges,
+                       w.num_tokens, w.max_num_tokens, T, B)
+    exp_s2, exp_e2 = oracle.slot_mapping_range(w.qsl, w.positions, lay.range_start, lay.range_len,
+                                               lay.num_ranges, w.num_tokens, w.max_num_tokens, T,
+                                               B)
+    assert e2 == exp_e2 and np.array_equal(s2, exp_s2) and np.array_equal(s2, exp_s)
+
+    L = 2
+    key = wl.bf16_normal((L, w.num_tokens, H, D), 20)
+    val = wl.bf16_normal((L, w.num_tokens, H, D), 21)
+    kc = wl.bf16_normal((L, B, T, H, D), 22)
+    vc = wl.bf16_normal((L, B, T, H, D), 23)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_we = oracle.cache_write(bits(key), bits(val), ek, ev, exp_s[:w.num_tokens], B, T)
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_cache_write(key.to(dev()), val.to(dev()), kc_d, vc_d, cuda(s[:w.num_tokens]), err=e)
+    assert int(e.item()) == exp_we
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+
+    for layer in range(L):
+        rows = int((w.gather_end - w.gather_start).sum())
+        ko = np.zeros((rows, H, D), np.uint16)
+        vo = np.zeros((rows, H, D), np.uint16)
+        exp_ge = oracle.cache_gather(ek, ev, layer, B, T, lay.table, w.gather_start, w.gather_end,
+                                     ko, vo)
+        e = err_word()
+        k_out, v_out = kv.kv_cache_gather(kc_d, vc_d, cuda(lay.table), cuda(w.gather_start),
+                                          cuda(w.gather_end), layer=layer, out_rows=rows, err=e)
+        assert int(e.item()) == exp_ge
+        assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
+        # gather of what was written gives the written tokens back
+        assert np.array_equal(bits(k_out), bits(key[layer]))
+
+
+# --------------------------------------------------- adversarial slot maps
+
+
+def random_slot_case(rng):
+    T = int(rng.choice([1, 4, 16, 32]))
+    R = int(rng.integers(0, 40))
+    lens = rng.integers(0, 70, size=R)
+    lens[rng.random(R) < 0.2] = 0
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    shift = int(rng.choice([0, 0, 0, 3]))
+    q = q + shift
+    N = int(q[-1]) + int(rng.choice([0, 0, 5]))
+    if rng.random() < 0.1 and R > 0:
+        q[-1] = max(q[-2], q[-1] - 2)
+    n_max = N + int(rng.choice([0, 1, 300]))
+    stride = int(rng.choice([0, 1, 8, 64]))
+    B = int(rng.integers(1, 300))
+    table = rng.integers(-1, B + 3, size=(max(R, 1), stride)).astype(np.int32)
+    table[rng.random(table.shape) < 0.2] = 0
+    pos = rng.integers(-2, max(stride, 1) * T + 20, size=N).astype(np.int64)
+    return T, R, q.astype(np.int32), N, n_max, stride, B, table, pos
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_paged_adversarial(seed):
+    rng = np.random.default_rng(1000 + seed)
+    T, R, q, N, n_max, stride, B, table, pos = random_slot_case(rng)
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
+    s, e = run_paged(q, pos, table, N, n_max, T, B)
+    assert e == exp_e
+    assert np.array_equal(s, exp_s)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_range_adversarial(seed):
+    rng = np.random.default_rng(2000 + seed)
+    T, R, q, N, n_max, stride, B, table, pos = random_slot_case(rng)
+    rstride = int(rng.choice([1, 4, 40, 256]))
+    rows = max(R, 1)
+    rs = rng.integers(-2, B + 2, size=(rows, rstride)).astype(np.int32)
+    rl = rng.integers(-1, 12, size=(rows, rstride)).astype(np.int32)
+    if rng.random() < 0.5:
+        rl = np.maximum(rl, 1)
+    nr = rng.integers(0, rstride + 1, size=rows).astype(np.int32)
+    if rng.random() < 0.3:
+        nr[rng.integers(0, rows)] = rstride + 1
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    s, e = run_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    assert e == exp_e
+    assert np.array_equal(s, exp_s)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_range_equals_paged_with_256_ranges(seed):
+    """Full descriptor rows (256 ranges, 8 warp chunks) agree with the table."""
+    rng = np.random.default_rng(3000 + seed)
+    T, R = 16, 3
+    rs = np.zeros((R, 256), np.int32)
+    rl = np.zeros((R, 256), np.int32)
+    nr = np.full(R, 256, np.int32)
+    lens = rng.integers(1, 6, size=(R, 256))
+    cursor = 1
+    for r in range(R):
+        for i in range(256):
+            rs[r, i] = cursor + int(rng.integers(0, 3))
+            rl[r, i] = lens[r, i]
+            cursor = rs[r, i] + lens[r, i]
+    B = cursor + 1
+    stride = wl.table_stride_for(int(lens.sum(axis=1).max()), T)
+    table = oracle.table_from_ranges(rs, rl, nr, stride)
+    tok = [int(rng.integers(1, 3000)) for _ in range(R)]
+    q = np.concatenate([[0], np.cumsum(tok)]).astype(np.int32)
+    pos = np.concatenate([rng.integers(0, int(lens[r].sum()) * T + 40, size=tok[r])
+                          for r in range(R)]).astype(np.int64)
+    N = int(q[-1])
+    sp, ep = run_paged(q, pos, table, N, N, T, B)
+    sr, er = run_range(q, pos, rs, rl, nr, N, N, T, B)
+    exp, ee = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+    assert ep == er == ee == 0
+    assert np.array_equal(sr, exp) and np.array_equal(sp, exp)
+
+
+def test_many_requests_qsl_in_global_memory():
+    rng = np.random.default_rng(7)
+    R, T = 9000, 16
+    lens = rng.integers(0, 3, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    table = rng.integers(0, 500, size=(R, 4)).astype(np.int32)
+    pos = rng.integers(0, 64, size=N).astype(np.int64)
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N + 7, T, 500)
+    s, e = run_paged(q, pos, table, N, N + 7, T, 500)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    rs = table.copy()
+    rl = np.ones_like(rs)
+    nr = np.full(R, 4, np.int32)
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N + 7, T, 500)
+    s, e = run_range(q, pos, rs, rl, nr, N, N + 7, T, 500)
+    assert e == exp_e and np.array_equal(s, exp_s)
+
+
+def test_malformed_qsl_sets_error_and_stays_in_bounds():
+    table = np.array([[1, 2], [3, 4]], np.int32)
+    q = [0, 5, 2]
+    pos = np.arange(5, dtype=np.int64)
+    s, e = run_paged(q, pos, table, 5, 6, 16, 8)
+    _, exp_e = oracle.slot_mapping_paged(q, pos, table, 5, 6, 16, 8)
+    assert e == exp_e and e & kv.ERR_BITS["BAD_QSL"]
+    assert s[5] == -1 and all(x == -1 or 16 <= x < 8 * 16 for x in s)
+
+
+def test_empty_slot_mappings():
+    s, e = run_paged([0], [], np.zeros((1, 4), np.int32), 0, 7, 16, 8)
+    assert e == 0 and s.tolist() == [-1] * 7
+    s, e = run_paged([0, 0, 0], [], np.zeros((2, 4), np.int32), 0, 0, 16, 8)
+    assert e == 0 and len(s) == 0
+    s, e = run_paged([0, 2, 1], [], np.zeros((2, 4), np.int32), 0, 0, 16, 8)
+    assert e == kv.ERR_BITS["BAD_QSL"]
+    z = np.zeros((1, 4), np.int32)
+    s, e = run_range([0], [], z, z, [0], 0, 3, 16, 8)
+    assert e == 0 and s.tolist() == [-1] * 3
+    s, e = run_range([0, 0], [], z, z, [9], 0, 0, 16, 8)
+    assert e == kv.ERR_BITS["BAD_RANGE"]
+
+
+# ------------------------------------------------------------------- write
+
+
+@pytest.mark.parametrize("H,D,L", [(8, 64, 1), (8, 128, 3), (1, 8, 2), (1, 128, 1), (16, 128, 2),
+                                   (32, 128, 1), (2, 72, 1)])
+def test_write_random_parity(H, D, L):
+    rng = np.random.default_rng(H * 1000 + D + L)
+    B, T, N = 37, 4, 61
+    slots = rng.permutation(np.arange(0, B * T))[:N].astype(np.int64)
+    slots[rng.random(N) < 0.15] = -1
+    slots[rng.integers(0, N)] = B * T + 5
+    slots[rng.integers(0, N)] = 1  # inside the null block
+    key = wl.bf16_normal((L, N, H, D), 30)
+    val = wl.bf16_normal((L, N, H, D), 31)
+    kc = wl.bf16_normal((L, B, T, H, D), 32)
+    vc = wl.bf16_normal((L, B, T, H, D), 33)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_e = oracle.cache_write(bits(key), bits(val), ek, ev, slots, B, T)
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_cache_write(key.to(dev()), val.to(dev()), kc_d, vc_d, cuda(slots), err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+
+
+def test_write_nothing_to_do():
+    kc = torch.zeros((1, 4, 16, 8, 64), dtype=torch.bfloat16, device=dev())
+    key = torch.zeros((1, 0, 8, 64), dtype=torch.bfloat16, device=dev())
+    e = err_word()
+    kv.kv_cache_write(key, key, kc, kc.clone(), torch.zeros(0, dtype=torch.int64, device=dev()),
+                      err=e)
+    assert int(e.item()) == 0 and int(kc.abs().sum().item()) == 0
+
+
+# ------------------------------------------------------------------ gather
+
+
+@pytest.mark.parametrize("seed,R,H,D", [(0, 1, 8, 128), (1, 5, 8, 64), (2, 300, 1, 8),
+                                        (3, 4096, 1, 16), (4, 17, 16, 128), (5, 9, 2, 72)])
+def test_gather_random_parity(seed, R, H, D):
+    rng = np.random.default_rng(4000 + seed)
+    T, B, L, stride = 8, 50, 2, 6
+    table = rng.integers(-1, B + 2, size=(R, stride)).astype(np.int32)
+    table[rng.random(table.shape) < 0.2] = 0
+    g0 = rng.integers(-1, stride * T, size=R).astype(np.int32)
+    g1 = (g0 + rng.integers(-2, 20, size=R)).astype(np.int32)
+    total = int(np.where((g0 >= 0) & (g1 >= g0), g1 - g0, 0).sum())
+    out_rows = max(0, total - int(rng.integers(0, 3))) if seed % 2 else total + 3
+    kc = wl.bf16_normal((L, B, T, H, D), 40 + seed)
+    vc = wl.bf16_normal((L, B, T, H, D), 50 + seed)
+    layer = seed % L
+    ko = np.full((out_rows, H, D), 0x1234, np.uint16)
+    vo = np.full((out_rows, H, D), 0x4321, np.uint16)
+    exp_e = oracle.cache_gather(bits(kc), bits(vc), layer, B, T, table, g0, g1, ko, vo)
+    k_out = torch.from_numpy(ko.view(np.int16).copy()).view(torch.bfloat16).to(dev())
+    v_out = torch.from_numpy(vo.view(np.int16).copy()).view(torch.bfloat16).to(dev())
+    e = err_word()
+    kv.kv_cache_gather(kc.to(dev()), vc.to(dev()), cuda(table), cuda(g0), cuda(g1), layer=layer,
+                       k_out=k_out, v_out=v_out, out_rows=out_rows, err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
+
+
+def test_gather_padding_rows_give_nothing():
+    kc = wl.bf16_normal((1, 8, 16, 8, 128), 60).to(dev())
+    table = torch.zeros((128, 64), dtype=torch.int32, device=dev())
+    zeros = torch.zeros(128, dtype=torch.int32, device=dev())
+    out = torch.empty((0, 8, 128), dtype=torch.bfloat16, device=dev())
+    e = err_word()
+    kv.kv_cache_gather(kc, kc, table, zeros, zeros, k_out=out, v_out=out, out_rows=0, err=e)
+    assert int(e.item()) == 0
+
+
+# ------------------------------------------------------------------ expand
+
+
+@pytest.mark.parametrize("k,extra", [(1, 0), (2, 0), (2, 3), (3, 1), (4, 4), (8, 0)])
+def test_expand_random_parity(k, extra):
+    rng = np.random.default_rng(5000 + k * 10 + extra)
+    R, Ms = 37, 19
+    mgr = rng.integers(-2, 1 << 20, size=(R, Ms)).astype(np.int32)
+    mgr[rng.random(mgr.shape) < 0.3] = 0
+    mgr[0, 0] = (1 << 31) // k if k > 1 else mgr[0, 0]
+    Ks = Ms * k + extra
+    exp, exp_e = oracle.expand_kernel_blocks(mgr, 16 * k, 16, Ks)
+    e = err_word()
+    out = kv.kv_expand_kernel_blocks(cuda(mgr), 16 * k, 16,
+                                     kernel_table=torch.full((R, Ks), 77, dtype=torch.int32,
+                                                             device=dev()), err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(out.cpu().numpy(), exp)
