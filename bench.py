@@ -1,0 +1,699 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step is one pass of the whole hot path over one synthetic batch.  The
+default workload is the decode step: 256 requests with one new token each,
+contexts U{512..4096}, block size 16, a 40960-block pool, 8 KV heads x 128
+bf16, each request's blocks in 1-4 contiguous ranges.  A step runs
+
+  1. kv_slot_mapping_paged   (block-table strategy)
+  2. kv_slot_mapping_range   (range strategy, same layout, side by side)
+  3. kv_cache_write          (the new tokens' K/V rows to their slots)
+  4. kv_cache_gather         (read path: every request's whole context,
+                              through its block table, into packed buffers)
+
+and `value` is new tokens per second over the whole job.  The L2 is flushed
+(a 256 MiB write) between timed steps, outside the timed events.  Rank 0
+prints one JSON line.  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload.  The other workloads (mixed
+prefill+decode over 32 layers, 128K-context gather, hybrid groups) are timed
+per kernel after the headline and reported under "configs".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "KV write+slot-map tokens/s and gather GB/s (frac of ~8 TB/s), paged vs range"
+FLUSH_BYTES = 256 << 20
+DECODE_DESC = ("decode step: 256 requests x 1 new token, context U{512..4096}, block_size 16, "
+               "40960-block pool, KV 8x128 bf16 (one layer), 1-4 contiguous ranges per request; "
+               "step = paged slot map + range slot map + KV write + context gather")
+
+
+# --------------------------------------------------------------------------
+# peaks, clocks, profile-derived traffic
+# --------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+_REASONS = [(0x1, "gpu_idle"), (0x2, "applications_clocks_setting"), (0x4, "sw_power_cap"),
+            (0x8, "hw_slowdown"), (0x10, "sync_boost"), (0x20, "sw_thermal_slowdown"),
+            (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"),
+            (0x100, "display_clock_setting")]
+
+
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons through NVML (read only)."""
+
+    def __init__(self, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._h = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            bus = self._bus_id()
+            ok = False
+            if bus:
+                ok = nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            if not ok and nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self._nvml, self._h = nvml, h
+            m = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = int(m.value)
+            self._reasons_fn = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except Exception:
+            self._nvml = None
+
+    @staticmethod
+    def _bus_id():
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(torch.cuda.current_device())
+            return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return None
+
+    def _loop(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if self._reasons_fn(self._h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        if self._nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = [n for bit, n in _REASONS if self.reasons & bit and n != "gpu_idle"]
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (its .cu file and the common header)."""
+    files = {"cache_gather_kernel": "kv_cache_gather.cu", "cache_write_kernel": "kv_cache_write.cu",
+             "slot_mapping_paged_kernel": "kv_slot_mapping.cu",
+             "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu"}
+    h = hashlib.sha256()
+    for f in (files[kernel], "kv_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[workload][kernel]
+        if e.get("source_sha256") != kernel_source_sha(kernel):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+# workloads as lists of launches
+# --------------------------------------------------------------------------
+
+class Launch:
+    """One timed call of the C ABI; `launches` kernels are enqueued per call."""
+
+    def __init__(self, name, kernel, fn, alg_bytes, units=0, launches=1):
+        self.name, self.kernel, self.fn, self.alg_bytes = name, kernel, fn, alg_bytes
+        self.units, self.launches = units, launches
+
+
+def _touched_blocks(g0, g1, T):
+    g0 = g0.astype(np.int64)
+    g1 = g1.astype(np.int64)
+    n = np.where(g1 > g0, (g1 - 1) // T - g0 // T + 1, 0)
+    return int(n.sum())
+
+
+def slotmap_bytes(N, n_max, R):
+    return n_max * 8 + N * 8 + N * 4 + (R + 1) * 4
+
+
+def range_bytes(N, n_max, R, nr):
+    return n_max * 8 + N * 8 + (R + 1) * 4 + R * 4 + int(nr[:R].sum()) * 8
+
+
+def write_bytes(L, N_valid, N, row_bytes):
+    return L * N_valid * row_bytes * 4 + N * 8
+
+
+def gather_bytes(rows, row_bytes, blocks, R):
+    return rows * row_bytes * 4 + blocks * 4 + R * 8
+
+
+class Built:
+    def __init__(self, name, desc, launches, tokens, keep):
+        self.name, self.desc, self.launches, self.tokens, self.keep = name, desc, launches, tokens, keep
+
+
+def build_decode(torch, kv, wl, dev, seed=1):
+    w = wl.decode(seed)
+    lay = w.layouts["G"]
+    T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qsl, pos, table = t(w.qsl), t(w.positions), t(lay.table)
+    rs, rl, nr = t(lay.range_start), t(lay.range_len), t(lay.num_ranges)
+    g0, g1 = t(w.gather_start), t(w.gather_end)
+    key = wl.bf16_normal((1, w.num_tokens, H, D), 11, dev)
+    val = wl.bf16_normal((1, w.num_tokens, H, D), 12, dev)
+    kc = wl.bf16_normal((1, B, T, H, D), 13, dev)
+    vc = wl.bf16_normal((1, B, T, H, D), 14, dev)
+    slot_p = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    slot_r = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = int((w.gather_end.astype(np.int64) - w.gather_start).sum())
+    k_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    N, n_max, R = w.num_tokens, w.max_num_tokens, w.num_reqs
+    rb = w.row_bytes
+    launches = [
+        Launch("slot_mapping_paged", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, table, T, B, max_num_tokens=n_max,
+                                                slot_mapping=slot_p, err=err),
+               slotmap_bytes(N, n_max, R), N),
+        Launch("slot_mapping_range", "slot_mapping_range_kernel",
+               lambda: kv.kv_slot_mapping_range(qsl, pos, rs, rl, nr, T, B, max_num_tokens=n_max,
+                                                slot_mapping=slot_r, err=err),
+               range_bytes(N, n_max, R, lay.num_ranges), N),
+        Launch("cache_write", "cache_write_kernel",
+               lambda: kv.kv_cache_write(key, val, kc, vc, slot_p, err=err),
+               write_bytes(1, N, N, rb), N),
+        Launch("cache_gather", "cache_gather_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, table, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err),
+               gather_bytes(rows, rb, _touched_blocks(w.gather_start, w.gather_end, T), R), rows),
+    ]
+    keep = dict(w=w, lay=lay, qsl=qsl, pos=pos, table=table, rs=rs, rl=rl, nr=nr, g0=g0, g1=g1,
+                key=key, val=val, kc=kc, vc=vc, slot_p=slot_p, slot_r=slot_r, err=err,
+                k_out=k_out, v_out=v_out, rows=rows)
+    return Built("decode", DECODE_DESC, launches, N, keep)
+
+
+def build_mixed(torch, kv, wl, dev, small=False):
+    free, _ = torch.cuda.mem_get_info(dev)
+    L = 1 if small else 32
+    w = wl.mixed()
+    note = ""
+    if not small and free < 2 * 32 * 49152 * 16 * 2048 + (8 << 30):
+        w = wl.mixed(num_blocks=32768, decode_ctx_max=2048)
+        note = " (reduced: 32768 blocks, decode ctx U{512..2048}, for free memory)"
+    lay = w.layouts["G"]
+    T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qsl, pos, table = t(w.qsl), t(w.positions), t(lay.table)
+    rs, rl, nr = t(lay.range_start), t(lay.range_len), t(lay.num_ranges)
+    key = wl.bf16_normal((L, w.num_tokens, H, D), 21, dev)
+    val = wl.bf16_normal((L, w.num_tokens, H, D), 22, dev)
+    kc = torch.full((L, B, T, H, D), 0x3C01, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    vc = torch.full((L, B, T, H, D), 0x3C01, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    slot_p = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    slot_r = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    N, n_max, R = w.num_tokens, w.max_num_tokens, w.num_reqs
+    launches = [
+        Launch("slot_mapping_paged", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, table, T, B, max_num_tokens=n_max,
+                                                slot_mapping=slot_p, err=err),
+               slotmap_bytes(N, n_max, R), N),
+        Launch("slot_mapping_range", "slot_mapping_range_kernel",
+               lambda: kv.kv_slot_mapping_range(qsl, pos, rs, rl, nr, T, B, max_num_tokens=n_max,
+                                                slot_mapping=slot_r, err=err),
+               range_bytes(N, n_max, R, lay.num_ranges), N),
+        Launch("cache_write", "cache_write_kernel",
+               lambda: kv.kv_cache_write(key, val, kc, vc, slot_p, err=err),
+               write_bytes(L, N, N, w.row_bytes), N * L),
+    ]
+    desc = (f"mixed prefill+decode: 16 prefill chunks (8192 tokens) + 240 decode tokens, "
+            f"{L} layers, {B}-block pool per layer, KV 8x128 bf16, 1-8 ranges/request{note}")
+    keep = dict(kc=kc, vc=vc, key=key, val=val, err=err)
+    return Built("mixed", desc, launches, N, keep)
+
+
+def build_long(torch, kv, wl, dev, small=False):
+    w = wl.long_context(num_reqs=2 if small else 8)
+    T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qsl, pos = t(w.qsl), t(w.positions)
+    tp, tg = t(w.layouts["P"].table), t(w.layouts["G"].table)
+    lg = w.layouts["G"]
+    rs, rl, nr = t(lg.range_start), t(lg.range_len), t(lg.num_ranges)
+    g0, g1 = t(w.gather_start), t(w.gather_end)
+    kc = wl.bf16_normal((1, B, T, H, D), 31, dev)
+    vc = wl.bf16_normal((1, B, T, H, D), 32, dev)
+    rows = w.num_tokens
+    k_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    slot = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    slot_pre = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    key = wl.bf16_normal((1, w.num_tokens, H, D), 33, dev)
+    val = wl.bf16_normal((1, w.num_tokens, H, D), 34, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    N, R = w.num_tokens, w.num_reqs
+    gb = gather_bytes(rows, w.row_bytes, _touched_blocks(w.gather_start, w.gather_end, T), R)
+    # the prompt's K/V written once (prefill) through the permuted table, so the
+    # write kernel also runs on inputs far larger than L2
+    kv.kv_slot_mapping_paged(qsl, pos, tp, T, B, slot_mapping=slot_pre, err=err)
+    launches = [
+        Launch("cache_write[prefill,P]", "cache_write_kernel",
+               lambda: kv.kv_cache_write(key, val, kc, vc, slot_pre, err=err),
+               write_bytes(1, N, N, w.row_bytes), N),
+        Launch("slot_mapping_paged[P]", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, tp, T, B, slot_mapping=slot, err=err),
+               slotmap_bytes(N, N, R), N),
+        Launch("slot_mapping_paged[G]", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, tg, T, B, slot_mapping=slot, err=err),
+               slotmap_bytes(N, N, R), N),
+        Launch("slot_mapping_range[G]", "slot_mapping_range_kernel",
+               lambda: kv.kv_slot_mapping_range(qsl, pos, rs, rl, nr, T, B, slot_mapping=slot,
+                                                err=err),
+               range_bytes(N, N, R, lg.num_ranges), N),
+        Launch("cache_gather[P]", "cache_gather_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tp, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err), gb, rows),
+        Launch("cache_gather[G]", "cache_gather_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err), gb, rows),
+    ]
+    desc = (f"long-context gather: {R} requests x 131072 tokens, block_size 16, KV 8x128 bf16; "
+            "P = permuted block table, G = 1-16 packed ranges per request; plus the prompt's "
+            "prefill write through P")
+    keep = dict(kc=kc, vc=vc, k_out=k_out, v_out=v_out, key=key, val=val, err=err)
+    return Built("long", desc, launches, N, keep)
+
+
+def build_hybrid(torch, kv, wl, dev, small=False):
+    h = wl.hybrid(num_real=128 if small else 512, num_padded=160 if small else 640)
+    H, D = h.num_kv_heads, h.head_dim
+    rb = H * D * 2
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qsl, pos = t(h.qsl), t(h.positions)
+    key = wl.bf16_normal((1, h.num_tokens, H, D), 41, dev)
+    val = wl.bf16_normal((1, h.num_tokens, H, D), 42, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    launches, keep = [], dict(key=key, val=val, err=err)
+    R, N, n_max = h.num_reqs, h.num_tokens, h.max_num_tokens
+    for name, g in h.groups.items():
+        kbs, mbs, Bk = g.kernel_block_size, g.mgr_block_size, g.kernel_num_blocks
+        k = mbs // kbs
+        mgr = t(g.mgr_table)
+        kt = torch.empty((R, g.mgr_table.shape[1] * k), dtype=torch.int32, device=dev)
+        kc = wl.bf16_normal((1, Bk, kbs, H, D), 43 + len(name), dev)
+        vc = wl.bf16_normal((1, Bk, kbs, H, D), 45 + len(name), dev)
+        slot = torch.empty(n_max, dtype=torch.int64, device=dev)
+        # gather calls: 64 real requests per call, then the padding rows in one call
+        calls = [(c, min(c + 64, h.num_real_reqs)) for c in range(0, h.num_real_reqs, 64)]
+        calls.append((h.num_real_reqs, R))
+        max_rows = max(int((g.gather_end[a:b].astype(np.int64) - g.gather_start[a:b]).sum())
+                       for a, b in calls)
+        k_out = torch.empty((max(max_rows, 1), H, D), dtype=torch.bfloat16, device=dev)
+        v_out = torch.empty((max(max_rows, 1), H, D), dtype=torch.bfloat16, device=dev)
+        g0, g1 = t(g.gather_start), t(g.gather_end)
+        keep.update({f"{name}_{x}": y for x, y in dict(mgr=mgr, kt=kt, kc=kc, vc=vc, slot=slot,
+                                                         k_out=k_out, v_out=v_out, g0=g0,
+                                                         g1=g1).items()})
+        rows_total = int((g.gather_end.astype(np.int64) - g.gather_start).sum())
+
+        def gather_all(kc=kc, vc=vc, kt=kt, g0=g0, g1=g1, k_out=k_out, v_out=v_out, calls=calls,
+                       g=g):
+            for a, b in calls:
+                rows = int((g.gather_end[a:b].astype(np.int64) - g.gather_start[a:b]).sum())
+                kv.kv_cache_gather(kc, vc, kt[a:b], g0[a:b], g1[a:b], k_out=k_out, v_out=v_out,
+                                   out_rows=rows, err=err)
+
+        launches += [
+            Launch(f"expand[{name}]", "expand_kernel",
+                   lambda mgr=mgr, kt=kt, mbs=mbs, kbs=kbs: kv.kv_expand_kernel_blocks(
+                       mgr, mbs, kbs, kernel_table=kt, err=err),
+                   g.mgr_table.size * 4 + R * g.mgr_table.shape[1] * k * 4, R),
+            Launch(f"slot_mapping_paged[{name}]", "slot_mapping_paged_kernel",
+                   lambda kt=kt, slot=slot, kbs=kbs, Bk=Bk: kv.kv_slot_mapping_paged(
+                       qsl, pos, kt, kbs, Bk, max_num_tokens=n_max, slot_mapping=slot, err=err),
+                   slotmap_bytes(N, n_max, R), N),
+            Launch(f"cache_write[{name}]", "cache_write_kernel",
+                   lambda kc=kc, vc=vc, slot=slot: kv.kv_cache_write(key, val, kc, vc, slot[:N],
+                                                                      err=err),
+                   write_bytes(1, N, N, rb), N),
+            Launch(f"cache_gather[{name}]", "cache_gather_kernel", gather_all,
+                   gather_bytes(rows_total, rb, _touched_blocks(g.gather_start, g.gather_end, kbs),
+                                R), rows_total, launches=len(calls)),
+        ]
+    desc = (f"hybrid groups: {h.num_real_reqs} requests padded to {R}, context U{{1..32768}}, "
+            "manager block 32 -> kernel block 16, full-attention + sliding-window 4096 groups, "
+            "KV 8x128 bf16; gather in calls of 64 requests + one call on the padding rows")
+    return Built("hybrid", desc, launches, N, keep)
+
+
+BUILDERS = {"decode": build_decode, "mixed": build_mixed, "long": build_long,
+            "hybrid": build_hybrid}
+
+
+# --------------------------------------------------------------------------
+# timing
+# --------------------------------------------------------------------------
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_steps(torch, built, steps, flush_buf, stream):
+    """Per-step and per-launch device times (ms) over `steps` steps, L2 flushed between."""
+    nl = len(built.launches)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(steps)]
+    for s in range(steps):
+        flush_l2(flush_buf)
+        evs[s][0].record(stream)
+        for i, l in enumerate(built.launches):
+            l.fn()
+            evs[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [evs[s][0].elapsed_time(evs[s][nl]) for s in range(steps)]
+    per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)] for i in range(nl)]
+    return step_ms, per
+
+
+def kernel_report(built, per, peak):
+    out = {}
+    for l, times in zip(built.launches, per):
+        avg = sum(times) / len(times)
+        gbs = l.alg_bytes / (avg * 1e-3) / 1e9
+        out[l.name] = {"us": round(avg * 1e3, 2), "us_median": round(statistics.median(times) * 1e3, 2),
+                       "alg_bytes": int(l.alg_bytes), "GB/s": round(gbs, 1),
+                       "frac_of_measured_hbm": round(gbs / peak, 4),
+                       "frac_of_8TBps": round(gbs / 8000.0, 4)}
+    return out
+
+
+# --------------------------------------------------------------------------
+# CPU oracle runs (baseline leg and reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req):
+    """One oracle pass of the decode step restricted to the first n_req requests."""
+    q = w.qsl[:n_req + 1]
+    n = int(q[-1])
+    pos = w.positions[:n]
+    sp, _ = oracle.slot_mapping_paged(q, pos, lay.table[:n_req], n, n, w.block_size, w.num_blocks)
+    oracle.slot_mapping_range(q, pos, lay.range_start[:n_req], lay.range_len[:n_req],
+                              lay.num_ranges[:n_req], n, n, w.block_size, w.num_blocks)
+    oracle.cache_write(key_h[:, :n], val_h[:, :n], kc_h, vc_h, sp, w.num_blocks, w.block_size)
+    g0, g1 = w.gather_start[:n_req], w.gather_end[:n_req]
+    rows = int((g1.astype(np.int64) - g0).sum())
+    ko = np.empty((rows, w.num_kv_heads, w.head_dim), np.uint16)
+    vo = np.empty_like(ko)
+    oracle.cache_gather(kc_h, vc_h, 0, w.num_blocks, w.block_size, lay.table[:n_req], g0, g1, ko,
+                        vo)
+    return n
+
+
+def host_decode_state(wl, seed=1):
+    w = wl.decode(seed)
+    lay = w.layouts["G"]
+    rng = np.random.default_rng(99)
+    shape = (1, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc_h = np.full(shape, 0x3C01, np.uint16)  # contents do not change the oracle's work
+    vc_h = np.full(shape, 0x3C02, np.uint16)
+    key_h = rng.integers(0, 1 << 16, size=(1, w.num_tokens, w.num_kv_heads, w.head_dim),
+                         dtype=np.uint16)
+    val_h = rng.integers(0, 1 << 16, size=key_h.shape, dtype=np.uint16)
+    return w, lay, kc_h, vc_h, key_h, val_h
+
+
+def cpu_baseline(seconds):
+    import oracle
+    from paged_kv_cache_39_gb300 import workloads as wl
+    w, lay, kc_h, vc_h, key_h, val_h = host_decode_state(wl)
+    oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 8)  # warm
+    t0 = time.perf_counter()
+    steps, toks = 0, 0
+    while True:
+        toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, w.num_reqs)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(toks / el, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} whole decode step(s) of the oracle (both slot maps, the write and "
+                      f"the {int((w.gather_end - w.gather_start).sum())}-row context gather), "
+                      f"single-threaded, {el:.1f} s",
+            "host_cores": os.cpu_count()}
+
+
+def run_reference(args, rk):
+    """The oracle as the reference arm, on bounded samples of the decode step."""
+    if not rk.is_main:
+        return
+    import oracle
+    from paged_kv_cache_39_gb300 import workloads as wl
+    w, lay, kc_h, vc_h, key_h, val_h = host_decode_state(wl)
+    t0 = time.perf_counter()
+    oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 4)
+    per_req = (time.perf_counter() - t0) / 4
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    n_req = int(max(1, min(w.num_reqs, budget / max(per_req, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req)
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req)
+    el = time.perf_counter() - t0
+    value = toks / el
+    sample = (f"each step: the oracle's decode step on the first {n_req} of 256 requests "
+              f"(both slot maps, write, context gather), single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": DECODE_DESC, "parallelism": "host cores, rank 0"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# end to end through the public API with host buffers
+# --------------------------------------------------------------------------
+
+def e2e_decode(torch, kv, built, steps, flush_buf, stream):
+    k = built.keep
+    w, lay = k["w"], k["lay"]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    host_in = {"qsl": pin(w.qsl), "pos": pin(w.positions), "table": pin(lay.table),
+               "rs": pin(lay.range_start), "rl": pin(lay.range_len), "nr": pin(lay.num_ranges),
+               "g0": pin(w.gather_start), "g1": pin(w.gather_end),
+               "key": k["key"].cpu().pin_memory(), "val": k["val"].cpu().pin_memory()}
+    host_out = {"slot_p": torch.empty_like(k["slot_p"], device="cpu").pin_memory(),
+                "slot_r": torch.empty_like(k["slot_r"], device="cpu").pin_memory(),
+                "err": torch.empty_like(k["err"], device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    times = []
+    for s in range(steps):
+        flush_l2(flush_buf)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for name, h in host_in.items():
+            k[name].copy_(h, non_blocking=True)
+        for l in built.launches:
+            l.fn()
+        for name, h in host_out.items():
+            h.copy_(k[name], non_blocking=True)
+        stream.synchronize()
+        times.append(time.perf_counter() - t0)
+    med = statistics.median(times)
+    return {"value": round(built.tokens / med, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(med * 1e3, 3),
+            "note": "median wall time of one step: pinned H2D of the step's inputs, the four "
+                    "calls, D2H of both slot mappings and the error word, stream synchronised"}
+
+
+# --------------------------------------------------------------------------
+# main
+# --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="decode", choices=list(BUILDERS))
+    ap.add_argument("--small", action="store_true",
+                    help="shrink the workload (profiling captures); not a bench line")
+    ap.add_argument("--no-detail", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--detail-reps", type=int, default=10)
+    args = ap.parse_args()
+    args.steps = max(1, args.steps)
+    args.warmup = max(3, args.warmup)
+
+    from paged_kv_cache_39_gb300 import dist as kdist
+    if args.impl == "reference":
+        run_reference(args, kdist.from_env())
+        return
+
+    import torch
+    import paged_kv_cache_39_gb300 as kv
+    from paged_kv_cache_39_gb300 import workloads as wl
+
+    rk = kdist.init("nccl")
+    dev = torch.device("cuda", rk.local_rank)
+    torch.cuda.set_device(dev)
+    kv.load()
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = load_peaks()
+    flush_buf = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    built = BUILDERS[args.workload](torch, kv, wl, dev, **({} if args.workload == "decode"
+                                                          else {"small": args.small}))
+    for _ in range(args.warmup):
+        flush_l2(flush_buf)
+        for l in built.launches:
+            l.fn()
+    torch.cuda.synchronize()
+    if int(built.keep["err"].item()) != 0:
+        raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
+
+    with ClockSampler() as clocks:
+        kdist.barrier(dev)
+        torch.cuda.synchronize()
+        step_ms, per = time_steps(torch, built, args.steps, flush_buf, stream)
+        torch.cuda.synchronize()
+        kdist.barrier(dev)
+    ms_per_step = sum(step_ms) / len(step_ms)
+    ms_max = kdist.max_over_ranks(ms_per_step, dev)
+    value = built.tokens * rk.world_size / (ms_max * 1e-3)
+    kernels = kernel_report(built, per, peak)
+
+    # dominant kernel of the step
+    dom_i = max(range(len(built.launches)), key=lambda i: sum(per[i]))
+    dom = built.launches[dom_i]
+    dom_avg_ms = sum(per[dom_i]) / len(per[dom_i])
+    achieved = dom.alg_bytes / (dom_avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(dom.kernel, args.workload)
+    roofline = {"bound": "hbm", "kernel": dom.kernel, "achieved": round(achieved, 1),
+                "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, read+write)",
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "alg_bytes_per_launch": int(dom.alg_bytes),
+                "avg_launch_us": round(dom_avg_ms * 1e3, 2)}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": rk.world_size, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "payload": "bf16 bits copied",
+            "data": "synthetic",
+            "config": {"workload": built.desc + (" [small]" if args.small else ""),
+                       "l2": "flushed between timed steps (256 MiB write outside the events)",
+                       "parallelism": "replicas" if rk.world_size > 1 else "single GPU",
+                       "per_gpu_tokens_per_step": built.tokens},
+            "kernels": kernels, "roofline": roofline,
+            "gpu_launches": args.steps * sum(l.launches for l in built.launches),
+            "clocks": clocks.summary()}
+    if built.name == "decode":
+        t_paged = kernels["slot_mapping_paged"]["us"]
+        t_range = kernels["slot_mapping_range"]["us"]
+        t_write = kernels["cache_write"]["us"]
+        line["write_slotmap_tokens_per_s"] = {
+            "paged": round(built.tokens / ((t_paged + t_write) * 1e-6), 1),
+            "range": round(built.tokens / ((t_range + t_write) * 1e-6), 1)}
+        line["gather_GBps"] = kernels["cache_gather"]["GB/s"]
+        line["e2e"] = e2e_decode(torch, kv, built, min(args.steps, 200), flush_buf, stream)
+
+    if rk.is_main and rk.world_size == 1:
+        if args.workload == "decode" and args.cpu_seconds > 0:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if not args.no_detail and args.workload == "decode":
+            built = None
+            torch.cuda.empty_cache()
+            line["configs"] = detail(torch, kv, wl, dev, args, flush_buf, stream, peak)
+    if rk.is_main:
+        print(json.dumps(line), flush=True)
+    kdist.finalize()
+
+
+def detail(torch, kv, wl, dev, args, flush_buf, stream, peak):
+    out = {}
+    for name in ("mixed", "long", "hybrid"):
+        b = BUILDERS[name](torch, kv, wl, dev)
+        for _ in range(3):
+            for l in b.launches:
+                l.fn()
+        torch.cuda.synchronize()
+        _, per = time_steps(torch, b, args.detail_reps, flush_buf, stream)
+        rep = kernel_report(b, per, peak)
+        entry = {"workload": b.desc, "kernels": rep, "errors": int(b.keep["err"].item())}
+        if name == "mixed":
+            tw = rep["cache_write"]["us"]
+            entry["write_slotmap_tokens_per_s"] = {
+                "paged": round(b.tokens / ((rep["slot_mapping_paged"]["us"] + tw) * 1e-6), 1),
+                "range": round(b.tokens / ((rep["slot_mapping_range"]["us"] + tw) * 1e-6), 1)}
+        out[name] = entry
+        del b
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    main()
