@@ -13,7 +13,8 @@ bf16, each request's blocks in 1-4 contiguous ranges.  A step runs
                               through its block table, into packed buffers)
 
 and `value` is new tokens per second over the whole job.  The L2 is flushed
-(a 256 MiB write) between timed steps, outside the timed events.  Rank 0
+(a 256 MiB write, then a 256 MiB read) between timed steps, outside the timed
+events.  Rank 0
 prints one JSON line.  `--impl reference` times the CPU oracle instead, on a
 bounded sample of the same workload.  The other workloads (mixed
 prefill+decode over 32 layers, 128K-context gather, hybrid groups) are timed
@@ -39,7 +40,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "KV write+slot-map tokens/s and gather GB/s (frac of ~8 TB/s), paged vs range"
-FLUSH_BYTES = 256 << 20
+FLUSH_BYTES = 512 << 20  # two halves of 256 MiB, each twice the 129 MB L2
 DECODE_DESC = ("decode step: 256 requests x 1 new token, context U{512..4096}, block_size 16, "
                "40960-block pool, KV 8x128 bf16 (one layer), 1-4 contiguous ranges per request; "
                "step = paged slot map + range slot map + KV write + context gather")
@@ -409,7 +410,12 @@ BUILDERS = {"decode": build_decode, "mixed": build_mixed, "long": build_long,
 # --------------------------------------------------------------------------
 
 def flush_l2(buf):
-    buf.add_(1)
+    """Write a buffer larger than L2, then read another one: the read evicts the
+    dirty lines the write left, so their write-back happens here and not
+    inside the next timed step."""
+    n = buf.numel() // 2
+    buf[:n].add_(1)
+    buf[n:].sum()
 
 
 def time_steps(torch, built, steps, flush_buf, stream):
@@ -644,7 +650,8 @@ def main():
             "vs_baseline": None, "dtype": "int64", "payload": "bf16 bits copied",
             "data": "synthetic",
             "config": {"workload": built.desc + (" [small]" if args.small else ""),
-                       "l2": "flushed between timed steps (256 MiB write outside the events)",
+                       "l2": "flushed between timed steps outside the events (256 MiB written, then "
+                                    "another 256 MiB read)",
                        "parallelism": "replicas" if rk.world_size > 1 else "single GPU",
                        "per_gpu_tokens_per_step": built.tokens},
             "kernels": kernels, "roofline": roofline,

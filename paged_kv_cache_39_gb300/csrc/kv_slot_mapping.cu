@@ -114,18 +114,21 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
 // sweep over every request, so the error word does not depend on which
 // descriptors the token loop happened to read.
 
+// Warp path: all needing lanes share request r0.  The count and the first 32
+// descriptors are requested together (`pre_s`, `pre_l`: descriptor `lane`,
+// loaded before the count is known), so the steady state costs one round trip.
 __device__ __forceinline__ void range_lookup_warp(const int32_t* __restrict__ rs,
                                                   const int32_t* __restrict__ rl, int nr,
-                                                  bool need, int64_t lb, int64_t& b_out,
-                                                  bool& found) {
+                                                  int32_t pre_s, int32_t pre_l, bool need,
+                                                  int64_t lb, int64_t& b_out, bool& found) {
   const int lane = threadIdx.x & 31;
   int64_t cum_base = 0;
   for (int c0 = 0; c0 < nr; c0 += 32) {
     const int i = c0 + lane;
     int32_t s = 0, len = 0;
     if (i < nr) {
-      s = rs[i];
-      len = max(rl[i], 0);
+      s = c0 == 0 ? pre_s : rs[i];
+      len = max(c0 == 0 ? pre_l : rl[i], 0);
     }
     const int64_t incl = warp_inclusive_scan<int64_t>((int64_t)len);
     const int64_t total = __shfl_sync(kFull, incl, 31);
@@ -151,6 +154,8 @@ __device__ __forceinline__ void range_lookup_warp(const int32_t* __restrict__ rs
     if (!__any_sync(kFull, need && !found)) break;
   }
 }
+
+constexpr int kLanePrefetch = 4;  // descriptors a lane requests with the count
 
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
@@ -186,13 +191,7 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
     // every lane of the warp reaches the shuffles below: no early exit here
-    const bool live = t < a.num_tokens;
-    int r = live ? request_of(q, a.num_reqs, t) : -1;
-    int nr = 0;
-    if (r >= 0) {
-      nr = num_ranges[r];
-      if (nr < 0 || nr > rstride) r = -1;  // malformed row: PAD (flagged by the sweep)
-    }
+    const int r = t < a.num_tokens ? request_of(q, a.num_reqs, t) : -1;
     bool need = false;
     if (r >= 0) {
       if (p[k] < 0) err |= KV_ERR_BAD_POSITION;
@@ -204,27 +203,51 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
     const unsigned needers = __ballot_sync(kFull, need);
     if (needers != 0u) {
       const int r0 = __shfl_sync(kFull, r, __ffs(needers) - 1);
-      const bool uniform = __all_sync(kFull, !need || r == r0);
-      if (uniform) {
-        const int nr0 = __shfl_sync(kFull, nr, __ffs(needers) - 1);
-        range_lookup_warp(range_start + (int64_t)r0 * rstride, range_len + (int64_t)r0 * rstride,
-                          nr0, need, lb, b, found);
+      if (__all_sync(kFull, !need || r == r0)) {
+        const int32_t* rs0 = range_start + (int64_t)r0 * rstride;
+        const int32_t* rl0 = range_len + (int64_t)r0 * rstride;
+        int32_t pre_s = 0, pre_l = 0;
+        if (lane < rstride) {
+          pre_s = rs0[lane];
+          pre_l = rl0[lane];
+        }
+        const int nr0 = num_ranges[r0];
+        if (nr0 >= 0 && nr0 <= rstride)  // malformed rows: PAD (flagged by the sweep)
+          range_lookup_warp(rs0, rl0, nr0, pre_s, pre_l, need, lb, b, found);
       } else if (need) {
         const int32_t* rs = range_start + (int64_t)r * rstride;
         const int32_t* rl = range_len + (int64_t)r * rstride;
-        int64_t cum = 0;
-        for (int i = 0; i < nr; ++i) {
-          const int64_t len = max(rl[i], 0);
-          if (lb < cum + len) {
-            b = (int64_t)rs[i] + (lb - cum);
-            found = true;
-            break;
+        int32_t pre_s[kLanePrefetch], pre_l[kLanePrefetch];
+#pragma unroll
+        for (int i = 0; i < kLanePrefetch; ++i) {
+          pre_s[i] = i < rstride ? rs[i] : 0;
+          pre_l[i] = i < rstride ? rl[i] : 0;
+        }
+        const int nr = num_ranges[r];
+        if (nr >= 0 && nr <= rstride) {
+          int64_t cum = 0;
+#pragma unroll
+          for (int i = 0; i < kLanePrefetch; ++i) {
+            if (!found && i < nr) {
+              const int64_t len = max(pre_l[i], 0);
+              if (lb < cum + len) {
+                b = (int64_t)pre_s[i] + (lb - cum);
+                found = true;
+              }
+              cum += len;
+            }
           }
-          cum += len;
+          for (int i = kLanePrefetch; !found && i < nr; ++i) {
+            const int64_t len = max(rl[i], 0);
+            if (lb < cum + len) {
+              b = (int64_t)rs[i] + (lb - cum);
+              found = true;
+            }
+            cum += len;
+          }
         }
       }
     }
-    (void)lane;
     if (t < a.max_num_tokens)
       a.slot_mapping[t] = found ? slot_of(b, p[k], a.block_size, a.num_blocks, err) : kPad;
   }
