@@ -1,7 +1,7 @@
 """CPU oracle of the paged KV-cache hot path (numpy front end over kv_oracle.c).
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
-the benchmark's CPU-baseline leg may import this package.  It shares no code
+the benchmark's CPU-baseline leg and reference arm may import this package.  It shares no code
 with the CUDA library and never imports it; both sides are fed by the seeded
 generators in ``paged_kv_cache_39_gb300.workloads``.
 
@@ -53,7 +53,10 @@ def _load():
         "orc_slot_mapping_paged": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P], ctypes.c_int),
         "orc_slot_mapping_range": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P],
                                    ctypes.c_int),
-        "orc_table_from_ranges": ([_P, _P, _P, _I32, _I32, _I32, _P], ctypes.c_int),
+        "orc_table_from_ranges": ([_P, _P, _P, _I32, _I32, _I32, _P, _P], ctypes.c_int),
+        "orc_gather_rows_range": ([_I32, _I64, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I64, _P, _P],
+                                  ctypes.c_int),
+        "orc_copy_blocks": ([_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I32, _P], ctypes.c_int),
         "orc_cache_write": ([_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P], ctypes.c_int),
         "orc_write_rows": ([_P, _I32, _I32, _I64, _I32, _P, _P], ctypes.c_int),
         "orc_gather_rows": ([_I32, _I64, _I32, _P, _I32, _P, _P, _I32, _I64, _P, _P], ctypes.c_int),
@@ -127,15 +130,18 @@ def slot_mapping_range(qsl, positions, range_start, range_len, num_ranges, num_t
     return out, int(err[0])
 
 
-def table_from_ranges(range_start, range_len, num_ranges, table_stride: int) -> np.ndarray:
+def table_from_ranges(range_start, range_len, num_ranges, table_stride: int,
+                      with_error: bool = False):
+    """Block table [rows, table_stride] expanded from the range descriptors."""
     rs = _c(range_start, np.int32)
     rl = _c(range_len, np.int32)
     nr = _c(num_ranges, np.int32)
     R = rs.shape[0]
     table = np.empty((R, table_stride), dtype=np.int32)
+    err = np.zeros(1, dtype=np.int32)
     _check(_load().orc_table_from_ranges(_ptr(rs), _ptr(rl), _ptr(nr), rs.shape[1], R,
-                                         table_stride, _ptr(table)))
-    return table
+                                         table_stride, _ptr(table), _ptr(err)))
+    return (table, int(err[0])) if with_error else table
 
 
 def cache_write(key, value, k_cache, v_cache, slot_mapping, num_blocks: int,
@@ -180,6 +186,38 @@ def gather_rows(layer: int, num_blocks: int, block_size: int, block_table, gathe
     _check(_load().orc_gather_rows(layer, num_blocks, block_size, _ptr(table), table.shape[1],
                                    _ptr(g0), _ptr(g1), len(g0), out_rows, _ptr(out), _ptr(err)))
     return out, int(err[0])
+
+
+def gather_rows_range(layer: int, num_blocks: int, block_size: int, range_start, range_len,
+                      num_ranges, gather_start, gather_end, out_rows: int) -> Tuple[np.ndarray, int]:
+    """Source row of each output row of the range-addressed gather."""
+    rs = _c(range_start, np.int32)
+    rl = _c(range_len, np.int32)
+    nr = _c(num_ranges, np.int32)
+    g0 = _c(gather_start, np.int32)
+    g1 = _c(gather_end, np.int32)
+    out = np.empty(out_rows, dtype=np.int64)
+    err = np.zeros(1, dtype=np.int32)
+    _check(_load().orc_gather_rows_range(layer, num_blocks, block_size, _ptr(rs), _ptr(rl),
+                                         _ptr(nr), rs.shape[1], _ptr(g0), _ptr(g1), len(g0),
+                                         out_rows, _ptr(out), _ptr(err)))
+    return out, int(err[0])
+
+
+def copy_blocks(k_cache, v_cache, src_blocks, dst_blocks) -> int:
+    """Copy whole blocks src -> dst in every layer of both caches (in place)."""
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint16 or not c.flags["C_CONTIGUOUS"] or c.ndim != 5:
+            raise ValueError("caches must be C-contiguous uint16 [L, B, T, H, D] arrays")
+    L, B, T, H, D = k_cache.shape
+    src = _c(src_blocks, np.int32)
+    dst = _c(dst_blocks, np.int32)
+    if len(src) != len(dst):
+        raise ValueError("src and dst differ in length")
+    err = np.zeros(1, dtype=np.int32)
+    _check(_load().orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), L, B, T, H, D, _ptr(src),
+                                   _ptr(dst), len(src), _ptr(err)))
+    return int(err[0])
 
 
 def cache_gather(k_cache, v_cache, layer: int, num_blocks: int, block_size: int, block_table,

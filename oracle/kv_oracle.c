@@ -1,10 +1,11 @@
 /*
  * kv_oracle.c -- plain, slow, single-threaded CPU oracle of the paged
  * KV-cache hot path (slot mapping, range slot mapping, KV write, block-table
- * gather, kernel-block expansion).
+ * gather, kernel-block expansion) and of its next steps (range expansion
+ * into a block table, range-addressed gather, copy-on-write block copy).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
- * the benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * the benchmark's CPU-baseline leg and reference arm may load this library.  It shares no code,
  * header or constant table with the CUDA library: every definition here is
  * written out again from the pages it cites.
  *
@@ -190,32 +191,43 @@ int orc_slot_mapping_range(const int32_t* qsl, const int64_t* positions,
 }
 
 /* Expansion of range descriptors into a block-table row: logical block
- * range_cum + j of range i is physical block range_start + j.  Used by the
- * invariant "range and table strategies agree slot for slot when the table is
- * built from the ranges" ([RNG] Benchmark Methodology).  Entries the ranges do
- * not reach stay the null block; malformed rows give an all-null row.       */
+ * range_cum + j of range i is physical block range_start + j.  This is what
+ * the range backend has to materialise for table-reading consumers ([RNG]
+ * Status: the per-step block-table copy is redundant once the ranges hold the
+ * layout; a range-expansion kernel can fill the table directly), and it is
+ * the table for which [RNG] Benchmark Methodology states that both slot
+ * mapping strategies agree.  Entries the ranges do not reach stay the null
+ * block.  READING: a malformed row (count outside [0, range_stride]) is all
+ * null with BAD_RANGE; a range of length <= 0 covers nothing and sets
+ * BAD_RANGE; ranges reaching past table_stride are cut there with
+ * OUT_OF_SPACE; an entry outside the int32 range is null with BAD_BLOCK.   */
 int orc_table_from_ranges(const int32_t* range_start, const int32_t* range_len,
                           const int32_t* num_ranges, int32_t range_stride, int32_t num_reqs,
-                          int32_t table_stride, int32_t* table)
+                          int32_t table_stride, int32_t* table, int32_t* err)
 {
     if (num_reqs < 0 || range_stride < 0 || table_stride < 0) return ORC_EINVAL;
+    if (range_stride > ORC_RANGE_CAP) return ORC_EUNSUPPORTED;
+    int32_t e = 0;
     for (int32_t r = 0; r < num_reqs; ++r) {
         int32_t* row = table + (int64_t)r * table_stride;
         for (int32_t c = 0; c < table_stride; ++c) row[c] = ORC_NULL_BLOCK;
         int32_t nr = num_ranges[r];
-        if (nr < 0 || nr > range_stride) continue;
+        if (nr < 0 || nr > range_stride) { e |= ORC_BAD_RANGE; continue; }
         int64_t range_cum = 0;
         for (int32_t i = 0; i < nr; ++i) {
             int64_t len = range_len[(int64_t)r * range_stride + i];
-            if (len <= 0) continue;
+            if (len <= 0) { e |= ORC_BAD_RANGE; continue; }
             for (int64_t j = 0; j < len; ++j) {
                 int64_t lb = range_cum + j;
-                if (lb < table_stride)
-                    row[lb] = (int32_t)((int64_t)range_start[(int64_t)r * range_stride + i] + j);
+                int64_t b = (int64_t)range_start[(int64_t)r * range_stride + i] + j;
+                if (lb >= table_stride) { e |= ORC_OUT_OF_SPACE; break; }
+                if (b < 0 || b > INT32_MAX) { e |= ORC_BAD_BLOCK; continue; }
+                row[lb] = (int32_t)b;
             }
             range_cum += len;
         }
     }
+    *err |= e;
     return ORC_OK;
 }
 
@@ -344,6 +356,100 @@ int orc_cache_gather(const uint16_t* k_cache, const uint16_t* v_cache, int32_t l
             v_out[o * E + x] = n >= 0 ? v_cache[n * E + x] : 0;
         }
     }
+    return ORC_OK;
+}
+
+/* --------------------------------------------------------------------- */
+/* Range-addressed read path ([RNG] The Direction, milestone M7: range
+ * arithmetic instead of block-table resolution in the read-path kernels;
+ * Status: profile the gather against sequential range access).  Same output
+ * as the table gather of section above, with the block of position p found
+ * from the request's ranges: physical_block = range_start +
+ * (p // block_size - range_cum) ([RNG] The Innovation).
+ * READING: a position no range covers is a zero row (as a null table entry);
+ * a malformed descriptor row gives zero rows for all its positions; BAD_RANGE
+ * is set for every malformed row r < num_reqs; a resolved block 0 is a zero
+ * row; a block outside [0, B) is a zero row with BAD_BLOCK; spans and
+ * out_rows as in the table gather.  Source rows as orc_gather_rows.        */
+int orc_gather_rows_range(int32_t layer, int64_t num_blocks, int32_t block_size,
+                          const int32_t* range_start, const int32_t* range_len,
+                          const int32_t* num_ranges, int32_t range_stride,
+                          const int32_t* gather_start, const int32_t* gather_end, int32_t num_reqs,
+                          int64_t out_rows, int64_t* src_rows, int32_t* err)
+{
+    if (layer < 0 || num_blocks < 1 || block_size <= 0 || range_stride < 0 || num_reqs < 0 ||
+        out_rows < 0)
+        return ORC_EINVAL;
+    if (range_stride > ORC_RANGE_CAP) return ORC_EUNSUPPORTED;
+    int32_t e = 0;
+    for (int64_t o = 0; o < out_rows; ++o) src_rows[o] = -2;
+    for (int32_t r = 0; r < num_reqs; ++r)
+        e |= range_row_errors(range_len + (int64_t)r * range_stride, num_ranges[r], range_stride);
+    int64_t o_r = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        int64_t s0 = gather_start[r], s1 = gather_end[r];
+        if (s0 < 0 || s1 < s0) { e |= ORC_BAD_POSITION; continue; }
+        const int32_t* rs = range_start + (int64_t)r * range_stride;
+        const int32_t* rl = range_len + (int64_t)r * range_stride;
+        int32_t nr = num_ranges[r];
+        for (int64_t p = s0; p < s1; ++p) {
+            int64_t o = o_r + (p - s0);
+            if (o >= out_rows) { e |= ORC_OUT_OF_SPACE; continue; }
+            src_rows[o] = -1;
+            if (nr < 0 || nr > range_stride) continue;
+            int64_t lb = p / block_size;
+            int64_t range_cum = 0;
+            for (int32_t i = 0; i < nr; ++i) {
+                int64_t len = rl[i] > 0 ? rl[i] : 0;
+                if (range_cum <= lb && lb < range_cum + len) {
+                    int64_t b = (int64_t)rs[i] + (lb - range_cum);
+                    if (b < 0 || b >= num_blocks) e |= ORC_BAD_BLOCK;
+                    else if (b != ORC_NULL_BLOCK)
+                        src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);
+                    break;
+                }
+                range_cum += len;
+            }
+        }
+        o_r += s1 - s0;
+    }
+    *err |= e;
+    return ORC_OK;
+}
+
+/* Batched block copy for copy-on-write ([VBM] Deep Dive 3: when a writer
+ * diverges from a shared block the manager allocates a fresh block and
+ * queues KVCacheBlockCopy(src, dst) so that the worker copies the KV data
+ * before the writer overwrites it).  READING: every layer's K and V block
+ * dst becomes a copy of block src, pairs in order; src outside [1, B) is
+ * skipped with BAD_BLOCK (block 0 holds no data); dst == 0 is skipped with
+ * NULL_WRITE; dst outside [0, B) is skipped with BAD_BLOCK.                */
+int orc_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_layers, int64_t num_blocks,
+                    int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                    int32_t* err)
+{
+    if (num_layers < 0 || num_blocks < 1 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || num_pairs < 0)
+        return ORC_EINVAL;
+    int64_t E = (int64_t)num_kv_heads * head_dim;
+    int32_t e = 0;
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        int64_t sb = src_blocks[i], db = dst_blocks[i];
+        if (sb <= ORC_NULL_BLOCK || sb >= num_blocks) { e |= ORC_BAD_BLOCK; continue; }
+        if (db == ORC_NULL_BLOCK) { e |= ORC_NULL_WRITE; continue; }
+        if (db < 0 || db >= num_blocks) { e |= ORC_BAD_BLOCK; continue; }
+        for (int32_t l = 0; l < num_layers; ++l)
+            for (int32_t t = 0; t < block_size; ++t) {
+                int64_t s = orc_coord(l, sb, t, num_blocks, block_size) * E;
+                int64_t d = orc_coord(l, db, t, num_blocks, block_size) * E;
+                for (int64_t x = 0; x < E; ++x) {
+                    k_cache[d + x] = k_cache[s + x];
+                    v_cache[d + x] = v_cache[s + x];
+                }
+            }
+    }
+    *err |= e;
     return ORC_OK;
 }
 

@@ -40,13 +40,32 @@ MUTANTS = [
     ("write_src_transposed", "int64_t src = ((int64_t)l * num_tokens + t) * E;",
      "int64_t src = ((int64_t)t * num_layers + l) * E;"),
     ("write_k_v_swapped", "k_cache[n * E + x] = key[src + x];", "k_cache[n * E + x] = value[src + x];"),
-    ("gather_offset_dropped", "o_r += s1 - s0;", "o_r += 0;"),
+    ("gather_offset_dropped",
+     "            src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);\n"
+     "        }\n        o_r += s1 - s0;",
+     "            src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);\n"
+     "        }\n        o_r += 0;"),
+    ("gather_range_offset_dropped", "                    break;\n                }\n"
+     "                range_cum += len;\n            }\n        }\n        o_r += s1 - s0;",
+     "                    break;\n                }\n"
+     "                range_cum += len;\n            }\n        }\n        o_r += 0;"),
     ("gather_v_from_k", "v_out[o * E + x] = n >= 0 ? v_cache[n * E + x] : 0;",
      "v_out[o * E + x] = n >= 0 ? k_cache[n * E + x] : 0;"),
-    ("gather_token_offset", "src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);",
-     "src_rows[o] = orc_coord(layer, b, (p + 1) % block_size, num_blocks, block_size);"),
+    ("gather_token_offset",
+     "            src_rows[o] = orc_coord(layer, b, p % block_size, num_blocks, block_size);\n        }",
+     "            src_rows[o] = orc_coord(layer, b, (p + 1) % block_size, num_blocks, block_size);\n"
+     "        }"),
     ("expand_formula", "out[c * k + j] = (int32_t)(m * k + j);", "out[c * k + j] = (int32_t)(m + j * k);"),
     ("expand_null_expanded", "            if (m == ORC_NULL_BLOCK) continue;\n", ""),
+    ("table_from_ranges_offset", "int64_t b = (int64_t)range_start[(int64_t)r * range_stride + i] + j;",
+     "int64_t b = (int64_t)range_start[(int64_t)r * range_stride + i] + j + 1;"),
+    ("gather_range_sign", "                    int64_t b = (int64_t)rs[i] + (lb - range_cum);",
+     "                    int64_t b = (int64_t)rs[i] + (lb + range_cum);"),
+    ("gather_range_rows_unvalidated",
+     "        e |= range_row_errors(range_len + (int64_t)r * range_stride, num_ranges[r], range_stride);",
+     "        (void)0;"),
+    ("copy_direction_swapped", "k_cache[d + x] = k_cache[s + x];", "k_cache[s + x] = k_cache[d + x];"),
+    ("copy_null_guard_dropped", "if (db == ORC_NULL_BLOCK) { e |= ORC_NULL_WRITE; continue; }", ""),
     ("expand_divisor_unchecked", "if (mgr_block_size % kernel_block_size != 0) return ORC_EUNSUPPORTED;", ""),
 ]
 

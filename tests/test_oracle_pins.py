@@ -186,18 +186,37 @@ def test_range_cap_fails_closed():
     assert ei.value.status == oracle.EUNSUPPORTED
 
 
-@pytest.mark.parametrize("seed", range(6))
+def _concat_blocks(starts, lens):
+    out = []
+    for s_, ln in zip(starts, lens):
+        out.extend(range(int(s_), int(s_) + max(int(ln), 0)))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(8))
 def test_table_from_ranges_matches_concatenation(seed):
     rng = _rng(200 + seed)
     R, S, stride = 4, 6, 12
     rs = rng.integers(1, 50, size=(R, S)).astype(np.int32)
     rl = rng.integers(-1, 4, size=(R, S)).astype(np.int32)
     nr = rng.integers(0, S + 1, size=R).astype(np.int32)
-    table = oracle.table_from_ranges(rs, rl, nr, stride)
+    if seed % 3 == 0:
+        nr[0] = S + 1  # malformed row
+    table, err = oracle.table_from_ranges(rs, rl, nr, stride, with_error=True)
+    exp_err = 0
     for r in range(R):
-        blocks = [b for s, ln in zip(rs[r, :nr[r]], rl[r, :nr[r]])
-                  for b in range(int(s), int(s) + max(int(ln), 0))][:stride]
+        if nr[r] > S:
+            exp_err |= BITS["BAD_RANGE"]
+            assert (table[r] == 0).all()
+            continue
+        if (rl[r, :nr[r]] <= 0).any():
+            exp_err |= BITS["BAD_RANGE"]
+        blocks = _concat_blocks(rs[r, :nr[r]], rl[r, :nr[r]])
+        if len(blocks) > stride:
+            exp_err |= BITS["OUT_OF_SPACE"]
+        blocks = blocks[:stride]
         assert table[r].tolist() == blocks + [0] * (stride - len(blocks))
+    assert err == exp_err
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "mixed"])
@@ -207,8 +226,9 @@ def test_range_equals_paged_on_expanded_table(name):
     for key, lay in w.layouts.items():
         if lay.range_start is None:
             continue
-        table = oracle.table_from_ranges(lay.range_start, lay.range_len, lay.num_ranges,
-                                         lay.table_stride)
+        table, terr = oracle.table_from_ranges(lay.range_start, lay.range_len, lay.num_ranges,
+                                               lay.table_stride, with_error=True)
+        assert terr == 0
         assert np.array_equal(table, lay.table), key
         a, ea = oracle.slot_mapping_paged(w.qsl, w.positions, table, w.num_tokens,
                                           w.max_num_tokens, w.block_size, w.num_blocks)
@@ -395,6 +415,104 @@ def test_gather_out_of_space_and_bad_spans():
     src, err3 = oracle.gather_rows(0, B, T, table, [0, 0], [3, 9], 13)
     assert err3 == BITS["BAD_POSITION"]
     assert src.tolist() == [4, 5, 6, 12, 13, 14, 15, 16, 17, 18, 19, -1, -2]
+
+
+# ------------------------------------------------- range-addressed gather
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_gather_range_matches_concatenated_blocks(seed):
+    """Source rows of the range gather: logical block lb of request r is element
+    lb of its concatenated ranges; the row index is numpy's own C-order index
+    of (layer, block, offset) in a [L, B, T] grid."""
+    rng = _rng(600 + seed)
+    T, B, L, R, S = int(rng.choice([1, 4, 16])), 60, 3, 5, 6
+    layer = int(rng.integers(0, L))
+    rs = rng.integers(-1, B + 2, size=(R, S)).astype(np.int32)
+    rl = rng.integers(-1, 5, size=(R, S)).astype(np.int32)
+    nr = rng.integers(0, S + 1, size=R).astype(np.int32)
+    if seed % 4 == 0:
+        nr[1] = S + 2
+    g0 = rng.integers(-1, 10 * T, size=R).astype(np.int32)
+    g1 = (g0 + rng.integers(-2, 12 * T, size=R)).astype(np.int32)
+    total = int(np.where((g0 >= 0) & (g1 >= g0), g1 - g0, 0).sum())
+    out_rows = total - (seed % 3)
+    src, err = oracle.gather_rows_range(layer, B, T, rs, rl, nr, g0, g1, max(out_rows, 0))
+    exp_err, o_r = 0, 0
+    exp = np.full(max(out_rows, 0), -2, np.int64)
+    for r in range(R):
+        if nr[r] > S or (rl[r, :max(nr[r], 0)] <= 0).any():
+            exp_err |= BITS["BAD_RANGE"]
+    for r in range(R):
+        if g0[r] < 0 or g1[r] < g0[r]:
+            exp_err |= BITS["BAD_POSITION"]
+            continue
+        blocks = _concat_blocks(rs[r, :nr[r]], rl[r, :nr[r]]) if nr[r] <= S else []
+        for p in range(int(g0[r]), int(g1[r])):
+            o = o_r + p - int(g0[r])
+            if o >= out_rows:
+                exp_err |= BITS["OUT_OF_SPACE"]
+                continue
+            lb = p // T
+            exp[o] = -1
+            if lb < len(blocks):
+                b = blocks[lb]
+                if b < 0 or b >= B:
+                    exp_err |= BITS["BAD_BLOCK"]
+                elif b != 0:
+                    exp[o] = np.ravel_multi_index((layer, b, p % T), (L, B, T))
+        o_r += int(g1[r]) - int(g0[r])
+    assert err == exp_err
+    assert np.array_equal(src, exp)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "long"])
+def test_gather_range_equals_table_gather(name):
+    w = wl.CONFIGS[name]()
+    lay = w.layouts["G"]
+    rows = int((w.gather_end.astype(np.int64) - w.gather_start).sum())
+    a, ea = oracle.gather_rows(0, w.num_blocks, w.block_size, lay.table, w.gather_start,
+                               w.gather_end, rows)
+    b, eb = oracle.gather_rows_range(0, w.num_blocks, w.block_size, lay.range_start, lay.range_len,
+                                     lay.num_ranges, w.gather_start, w.gather_end, rows)
+    assert ea == eb == 0
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------- copy-on-write
+
+
+def test_copy_blocks_matches_slice_assignment():
+    rng = _rng(700)
+    L, B, T, H, D = 3, 20, 4, 2, 8
+    kc = _cache((L, B, T, H, D), 70)
+    vc = _cache((L, B, T, H, D), 71)
+    src = np.array([3, 5, 0, 7, 9, 2, 4], np.int32)
+    dst = np.array([11, 12, 13, 0, 25, 14, 15], np.int32)
+    ek, ev = kc.copy(), vc.copy()
+    for a_, b_ in zip(src, dst):
+        if 0 < a_ < B and 0 < b_ < B:
+            ek[:, b_] = ek[:, a_]
+            ev[:, b_] = ev[:, a_]
+    err = oracle.copy_blocks(kc, vc, src, dst)
+    assert err == BITS["BAD_BLOCK"] | BITS["NULL_WRITE"]
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+    assert np.array_equal(kc[:, 0], _cache((L, B, T, H, D), 70)[:, 0])  # null block kept
+
+
+def test_copy_blocks_then_write_diverges_only_the_copy():
+    """Copy-on-write: after copying a shared block and writing into the copy,
+    the original block is unchanged and the copy differs in one row."""
+    L, B, T, H, D = 2, 10, 4, 1, 8
+    kc = _cache((L, B, T, H, D), 72)
+    vc = _cache((L, B, T, H, D), 73)
+    orig = kc.copy()
+    assert oracle.copy_blocks(kc, vc, [4], [8]) == 0
+    key = _cache((L, 1, H, D), 74)
+    assert oracle.cache_write(key, key, kc, vc, np.array([8 * T + 2], np.int64), B, T) == 0
+    assert np.array_equal(kc[:, 4], orig[:, 4])
+    diff = (kc[:, 8] != orig[:, 4]).any(axis=(2, 3))
+    assert diff.tolist() == [[False, False, True, False]] * L
 
 
 # ----------------------------------------------------------------- expand
