@@ -141,7 +141,10 @@ def kernel_source_sha(kernel: str) -> str:
     """Hash of the sources a kernel is built from (its .cu file and the common header)."""
     files = {"cache_gather_kernel": "kv_cache_gather.cu", "cache_write_kernel": "kv_cache_write.cu",
              "slot_mapping_paged_kernel": "kv_slot_mapping.cu",
-             "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu"}
+             "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu",
+             "cache_gather_range_kernel": "kv_cache_gather.cu",
+             "table_from_ranges_kernel": "kv_range_table.cu",
+             "copy_blocks_kernel": "kv_copy_blocks.cu"}
     h = hashlib.sha256()
     for f in (files[kernel], "kv_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc", f), "rb") as fh:
@@ -204,7 +207,7 @@ class Built:
         self.name, self.desc, self.launches, self.tokens, self.keep = name, desc, launches, tokens, keep
 
 
-def build_decode(torch, kv, wl, dev, seed=1):
+def build_decode(torch, kv, wl, dev, seed=1, extras=False):
     w = wl.decode(seed)
     lay = w.layouts["G"]
     T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
@@ -241,6 +244,17 @@ def build_decode(torch, kv, wl, dev, seed=1):
                                           out_rows=rows, err=err),
                gather_bytes(rows, rb, _touched_blocks(w.gather_start, w.gather_end, T), R), rows),
     ]
+    if extras:
+        table2 = torch.empty_like(table)
+        launches += [
+            Launch("table_from_ranges", "table_from_ranges_kernel",
+                   lambda: kv.kv_table_from_ranges(rs, rl, nr, block_table=table2, err=err),
+                   lay.table.size * 4 + int(lay.num_ranges.sum()) * 8 + R * 4, R),
+            Launch("cache_gather_range", "cache_gather_range_kernel",
+                   lambda: kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, k_out=k_out,
+                                                    v_out=v_out, out_rows=rows, err=err),
+                   rows * rb * 4 + int(lay.num_ranges.sum()) * 8 + R * 12, rows),
+        ]
     keep = dict(w=w, lay=lay, qsl=qsl, pos=pos, table=table, rs=rs, rl=rl, nr=nr, g0=g0, g1=g1,
                 key=key, val=val, kc=kc, vc=vc, slot_p=slot_p, slot_r=slot_r, err=err,
                 k_out=k_out, v_out=v_out, rows=rows)
@@ -268,6 +282,10 @@ def build_mixed(torch, kv, wl, dev, small=False):
     slot_r = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     N, n_max, R = w.num_tokens, w.max_num_tokens, w.num_reqs
+    # copy-on-write fork of 1024 blocks (every layer): disjoint sources and targets
+    perm = np.random.default_rng(5).permutation(np.arange(1, B, dtype=np.int32))
+    n_cow = 1024
+    cow_src, cow_dst = t(perm[:n_cow]), t(perm[n_cow:2 * n_cow])
     launches = [
         Launch("slot_mapping_paged", "slot_mapping_paged_kernel",
                lambda: kv.kv_slot_mapping_paged(qsl, pos, table, T, B, max_num_tokens=n_max,
@@ -280,6 +298,9 @@ def build_mixed(torch, kv, wl, dev, small=False):
         Launch("cache_write", "cache_write_kernel",
                lambda: kv.kv_cache_write(key, val, kc, vc, slot_p, err=err),
                write_bytes(L, N, N, w.row_bytes), N * L),
+        Launch("copy_blocks[cow 1024]", "copy_blocks_kernel",
+               lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err),
+               n_cow * L * T * w.row_bytes * 4 + n_cow * 8, n_cow * L),
     ]
     desc = (f"mixed prefill+decode: 16 prefill chunks (8192 tokens) + 240 decode tokens, "
             f"{L} layers, {B}-block pool per layer, KV 8x128 bf16, 1-8 ranges/request{note}")
@@ -296,6 +317,7 @@ def build_long(torch, kv, wl, dev, small=False):
     lg = w.layouts["G"]
     rs, rl, nr = t(lg.range_start), t(lg.range_len), t(lg.num_ranges)
     g0, g1 = t(w.gather_start), t(w.gather_end)
+    tg_rebuilt = torch.empty_like(tg)
     kc = wl.bf16_normal((1, B, T, H, D), 31, dev)
     vc = wl.bf16_normal((1, B, T, H, D), 32, dev)
     rows = w.num_tokens
@@ -331,6 +353,13 @@ def build_long(torch, kv, wl, dev, small=False):
         Launch("cache_gather[G]", "cache_gather_kernel",
                lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
                                           out_rows=rows, err=err), gb, rows),
+        Launch("cache_gather_range[G]", "cache_gather_range_kernel",
+               lambda: kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, k_out=k_out,
+                                                v_out=v_out, out_rows=rows, err=err),
+               rows * w.row_bytes * 4 + int(lg.num_ranges.sum()) * 8 + R * 12, rows),
+        Launch("table_from_ranges[G]", "table_from_ranges_kernel",
+               lambda: kv.kv_table_from_ranges(rs, rl, nr, block_table=tg_rebuilt, err=err),
+               lg.table.size * 4 + int(lg.num_ranges.sum()) * 8 + R * 4, R),
     ]
     desc = (f"long-context gather: {R} requests x 131072 tokens, block_size 16, KV 8x128 bf16; "
             "P = permuted block table, G = 1-16 packed ranges per request; plus the prompt's "
@@ -401,8 +430,37 @@ def build_hybrid(torch, kv, wl, dev, small=False):
     return Built("hybrid", desc, launches, N, keep)
 
 
+def build_slotmap(torch, kv, wl, dev, small=False):
+    """The long-context slot maps alone (1M positions, no caches): a small
+    device footprint for full profiler captures of the two strategies."""
+    w = wl.long_context(num_reqs=2 if small else 8)
+    T, B = w.block_size, w.num_blocks
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    qsl, pos = t(w.qsl), t(w.positions)
+    tp, tg = t(w.layouts["P"].table), t(w.layouts["G"].table)
+    lg = w.layouts["G"]
+    rs, rl, nr = t(lg.range_start), t(lg.range_len), t(lg.num_ranges)
+    slot = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    N, R = w.num_tokens, w.num_reqs
+    launches = [
+        Launch("slot_mapping_paged[P]", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, tp, T, B, slot_mapping=slot, err=err),
+               slotmap_bytes(N, N, R), N),
+        Launch("slot_mapping_paged[G]", "slot_mapping_paged_kernel",
+               lambda: kv.kv_slot_mapping_paged(qsl, pos, tg, T, B, slot_mapping=slot, err=err),
+               slotmap_bytes(N, N, R), N),
+        Launch("slot_mapping_range[G]", "slot_mapping_range_kernel",
+               lambda: kv.kv_slot_mapping_range(qsl, pos, rs, rl, nr, T, B, slot_mapping=slot,
+                                                err=err),
+               range_bytes(N, N, R, lg.num_ranges), N),
+    ]
+    desc = f"long-context slot maps only: {R} requests x 131072 positions, block_size 16"
+    return Built("slotmap", desc, launches, N, dict(err=err))
+
+
 BUILDERS = {"decode": build_decode, "mixed": build_mixed, "long": build_long,
-            "hybrid": build_hybrid}
+            "hybrid": build_hybrid, "slotmap": build_slotmap}
 
 
 # --------------------------------------------------------------------------
@@ -681,8 +739,9 @@ def main():
 
 def detail(torch, kv, wl, dev, args, flush_buf, stream, peak):
     out = {}
-    for name in ("mixed", "long", "hybrid"):
-        b = BUILDERS[name](torch, kv, wl, dev)
+    for name in ("decode", "mixed", "long", "hybrid"):
+        b = (build_decode(torch, kv, wl, dev, extras=True) if name == "decode"
+             else BUILDERS[name](torch, kv, wl, dev))
         for _ in range(3):
             for l in b.launches:
                 l.fn()

@@ -1,12 +1,15 @@
 /*
  * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
  *
- * Five calls, each one kernel launch on the caller's stream:
+ * Eight calls, each one kernel launch on the caller's stream:
  *   kv_slot_mapping_paged    token -> cache slot through a block table
  *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
  *   kv_cache_write           scatter new K/V rows into the paged caches
  *   kv_cache_gather          gather a request's K/V through its block table
  *   kv_expand_kernel_blocks  manager-size block table -> kernel-size blocks
+ *   kv_table_from_ranges     range descriptors -> block table
+ *   kv_cache_gather_range    the gather, with blocks found from ranges
+ *   kv_copy_blocks           copy-on-write copy of whole blocks
  *
  * Sources (page title, section):
  *   [BT]  "Blocktabelle" (vLLM v0.25.1 walkthrough)
@@ -68,13 +71,13 @@ enum kv_error_bits {
     KV_ERR_BAD_RANGE = 8,     /* descriptor count outside [0, range_stride] or a range length <= 0 */
     KV_ERR_NULL_WRITE = 16,   /* write slot inside the null block 0 */
     KV_ERR_BAD_QSL = 32,      /* query_start_loc decreasing, negative, or past num_tokens */
-    KV_ERR_OUT_OF_SPACE = 64  /* gather output rows exceed out_rows */
+    KV_ERR_OUT_OF_SPACE = 64  /* gather rows exceed out_rows, or ranges exceed a table row */
 };
 
 #define KV_PAD_SLOT_ID (-1)
 #define KV_NULL_BLOCK_ID 0
 #define KV_MAX_RANGES_PER_REQ 256   /* [RNG] The Fork Implementation: capped at 256 ranges */
-#define KV_MAX_GATHER_REQS 4096     /* requests per kv_cache_gather call */
+#define KV_MAX_GATHER_REQS 4096     /* requests per kv_cache_gather(_range) call */
 
 /*
  * kv_slot_mapping_paged -- per-token cache slot through the block table.
@@ -228,6 +231,86 @@ int kv_expand_kernel_blocks(const int32_t* mgr_table, int32_t num_reqs, int32_t 
                             int32_t mgr_block_size, int32_t kernel_block_size,
                             int32_t* kernel_table, int32_t kernel_stride, int32_t* d_err,
                             kv_stream_t stream);
+
+/*
+ * kv_table_from_ranges -- materialise a block table from range descriptors.
+ *
+ * "Range-addressed KV cache blocks ...", Status: in range mode the staged
+ * block table is copied to the kernels' table every step although the range
+ * tables already hold the layout; a range-expansion kernel fills the table
+ * directly.  Row r gets, in logical order, the blocks of request r's ranges:
+ * logical block cum_i + j is range_start[r][i] + j (The Innovation).
+ *
+ *   range_start, range_len, num_ranges, range_stride  as kv_slot_mapping_range.
+ *   block_table  int32 [num_reqs, table_stride], written entirely.
+ *
+ * Columns past the ranges are the null block 0.  A row with num_ranges[r]
+ * outside [0, range_stride] is all null with KV_ERR_BAD_RANGE; a range with
+ * length <= 0 covers nothing and sets KV_ERR_BAD_RANGE; ranges reaching past
+ * table_stride are cut there with KV_ERR_OUT_OF_SPACE; an entry outside the
+ * int32 range is null with KV_ERR_BAD_BLOCK.  kv_slot_mapping_paged on the
+ * result equals kv_slot_mapping_range on the descriptors whenever no range is
+ * cut.
+ * Errors: KV_EINVAL for negative sizes or null/misaligned pointers with work
+ * to do; KV_EUNSUPPORTED for range_stride > KV_MAX_RANGES_PER_REQ.
+ */
+int kv_table_from_ranges(const int32_t* range_start, const int32_t* range_len,
+                         const int32_t* num_ranges, int32_t range_stride, int32_t num_reqs,
+                         int32_t* block_table, int32_t table_stride, int32_t* d_err,
+                         kv_stream_t stream);
+
+/*
+ * kv_cache_gather_range -- kv_cache_gather with the blocks found from range
+ * descriptors instead of a block table (range arithmetic on the read path:
+ * "Range-addressed KV cache blocks ...", The Direction, milestone M7, and the
+ * planned comparison of the table gather against sequential range access in
+ * Status).
+ *
+ * Arguments as kv_cache_gather, with (range_start, range_len, num_ranges,
+ * range_stride) as in kv_slot_mapping_range in place of the table.  Output
+ * rows, packing, spans, out_rows and the zero-row rules are those of
+ * kv_cache_gather, where "table entry" reads "the block range arithmetic
+ * gives": a logical block no range covers is a zero row (no error, like a
+ * null entry); every row r < num_reqs with a malformed descriptor row sets
+ * KV_ERR_BAD_RANGE and yields zero rows.  Equal to kv_cache_gather on the
+ * table kv_table_from_ranges builds whenever every requested position lies
+ * inside that table's stride.
+ * Errors: as kv_cache_gather; range_stride > KV_MAX_RANGES_PER_REQ is
+ * KV_EUNSUPPORTED.
+ */
+int kv_cache_gather_range(const void* k_cache, const void* v_cache, int32_t layer,
+                          int32_t num_layers, int64_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, const int32_t* range_start,
+                          const int32_t* range_len, const int32_t* num_ranges,
+                          int32_t range_stride, const int32_t* gather_start,
+                          const int32_t* gather_end, int32_t num_reqs, void* k_out, void* v_out,
+                          int64_t out_rows, int32_t* d_err, kv_stream_t stream);
+
+/*
+ * kv_copy_blocks -- batched whole-block copy for copy-on-write ("vLLM Block
+ * Table Management", Deep Dive 3: KVCacheBlockCopy(src, dst) is queued so the
+ * worker copies the KV data of a shared block into a fresh one before the
+ * writer overwrites it).
+ *
+ *   k_cache, v_cache  bf16 [num_layers, num_blocks, block_size, kv_heads, head_dim],
+ *                     read and written in place.
+ *   src_blocks, dst_blocks  int32 [num_pairs].
+ *
+ * For every pair i and layer l, block dst_blocks[i] of K and of V becomes a
+ * bit copy of block src_blocks[i].  A source outside [1, num_blocks) is
+ * skipped with KV_ERR_BAD_BLOCK (block 0 holds no data); a destination 0 is
+ * skipped with KV_ERR_NULL_WRITE; a destination outside [0, num_blocks) is
+ * skipped with KV_ERR_BAD_BLOCK.  Destinations must be distinct and no
+ * destination may be the source of another pair (as for freshly allocated
+ * copy targets); otherwise copies race.  num_layers == 0 reads, writes and
+ * checks nothing.
+ * Errors: KV_EINVAL as kv_cache_write; KV_EUNSUPPORTED for a row size not a
+ * multiple of 16 bytes.
+ */
+int kv_copy_blocks(void* k_cache, void* v_cache, int32_t num_layers, int64_t num_blocks,
+                   int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                   const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
+                   int32_t* d_err, kv_stream_t stream);
 
 /* Human-readable name of a kv_status value (static string). */
 const char* kv_status_string(int status);

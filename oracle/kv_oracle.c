@@ -434,6 +434,7 @@ int orc_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int32_t num_layers, in
         return ORC_EINVAL;
     int64_t E = (int64_t)num_kv_heads * head_dim;
     int32_t e = 0;
+    if (num_layers == 0) return ORC_OK;  /* nothing to read, write or check */
     for (int32_t i = 0; i < num_pairs; ++i) {
         int64_t sb = src_blocks[i], db = dst_blocks[i];
         if (sb <= ORC_NULL_BLOCK || sb >= num_blocks) { e |= ORC_BAD_BLOCK; continue; }

@@ -42,6 +42,10 @@ SIGNATURES = {
     "kv_cache_gather": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P, _P,
                          _I64, _P, _P], ctypes.c_int),
     "kv_expand_kernel_blocks": ([_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _P], ctypes.c_int),
+    "kv_table_from_ranges": ([_P, _P, _P, _I32, _I32, _P, _I32, _P, _P], ctypes.c_int),
+    "kv_cache_gather_range": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P,
+                               _I32, _P, _P, _I64, _P, _P], ctypes.c_int),
+    "kv_copy_blocks": ([_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P], ctypes.c_int),
     "kv_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "kv_abi_version": ([], ctypes.c_int),
 }

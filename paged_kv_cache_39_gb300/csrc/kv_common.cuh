@@ -43,6 +43,37 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                : "memory");
 }
 
+// Quotient and remainder of a non-negative position by the block size: a
+// shift and a mask when the block size is a power of two (the usual 16 or
+// 32), a 32-bit division when the position fits, else a 64-bit division.
+struct BlockDiv {
+  int32_t size;
+  int32_t shift;  // log2(size) when size is a power of two, else -1
+
+  static BlockDiv make(int32_t size) {
+    int32_t sh = -1;
+    if (size > 0 && (size & (size - 1)) == 0) {
+      sh = 0;
+      while ((1 << sh) != size) ++sh;
+    }
+    return BlockDiv{size, sh};
+  }
+
+  __device__ __forceinline__ void divmod(int64_t p, int64_t& q, int64_t& r) const {
+    if (shift >= 0) {
+      q = p >> shift;
+      r = p & (size - 1);
+    } else if (p <= 0x7fffffff) {
+      const uint32_t pu = (uint32_t)p, qu = pu / (uint32_t)size;
+      q = qu;
+      r = pu - qu * (uint32_t)size;
+    } else {
+      q = p / size;
+      r = p - q * size;
+    }
+  }
+};
+
 // Largest r in [0, n) with q[r] <= t, or -1: the request whose span starts
 // at or before token t (q is a non-decreasing query_start_loc).
 __device__ __forceinline__ int find_span(const int32_t* q, int n, int32_t t) {

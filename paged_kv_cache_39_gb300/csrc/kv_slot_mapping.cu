@@ -9,9 +9,11 @@
 //
 // GPU shape.  The pages' kernel runs one program per request and walks its
 // tokens, which leaves a 128K-token request on one SM.  Here a CTA owns a
-// fixed tile of 1024 consecutive tokens (4 per thread, coalesced), so the
-// grid depends only on max_num_tokens (stable under CUDA-graph capture) and
-// long prefills spread over every SM.  Each thread finds its request by a
+// fixed tile of 256 x TPT consecutive tokens (TPT per thread, coalesced, all
+// of a thread's loads in flight together), so the grid depends only on
+// max_num_tokens (stable under CUDA-graph capture) and long prefills spread
+// over every SM; TPT grows from 4 to 16 with the batch so that the grid stays
+// within one wave of resident CTAs.  Each thread finds its request by a
 // binary search of query_start_loc staged in shared memory.  The tail
 // [num_tokens, max_num_tokens) is just more tiles that store PAD.
 #include "kv_common.cuh"
@@ -20,14 +22,13 @@ namespace kvp {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTokPerThread = 4;
-constexpr int kTile = kThreads * kTokPerThread;
 constexpr int kQslSmemMax = 8192;  // int32 entries of query_start_loc staged in smem
 
 struct SlotArgs {
   const int32_t* qsl;
   const int64_t* positions;
-  int32_t num_reqs, num_tokens, max_num_tokens, block_size;
+  int32_t num_reqs, num_tokens, max_num_tokens;
+  BlockDiv bs;
   int64_t num_blocks;
   int64_t* slot_mapping;
   int32_t* err;
@@ -58,19 +59,30 @@ __device__ __forceinline__ int request_of(const int32_t* q, int n, int32_t t) {
   return (r >= 0 && t < q[r + 1]) ? r : -1;
 }
 
-// Final check of a resolved physical block and the slot it gives.
-__device__ __forceinline__ int64_t slot_of(int64_t b, int64_t p, int32_t T, int64_t B,
+// Same, trying the thread's previous request first: a thread's tokens are
+// 256 apart, so inside a long prefill they keep falling in one span.
+__device__ __forceinline__ int request_of_cached(const int32_t* q, int n, int32_t t, int& last) {
+  if (last >= 0 && t >= q[last] && t < q[last + 1]) return last;
+  const int r = request_of(q, n, t);
+  if (r >= 0) last = r;
+  return r;
+}
+
+// Final check of a resolved physical block and the slot it gives (off is
+// the position's offset inside its block).
+__device__ __forceinline__ int64_t slot_of(int64_t b, int64_t off, int32_t T, int64_t B,
                                            uint32_t& err) {
   if (b == kNull) return kPad;
   if (b < 0 || b >= B) { err |= KV_ERR_BAD_BLOCK; return kPad; }
-  return b * T + p % T;
+  return b * T + off;
 }
 
+template <int kTokPerThread>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t stride,
                           bool qsl_in_smem) {
   extern __shared__ int32_t s_qsl[];
-  const int32_t base = blockIdx.x * kTile + threadIdx.x;
+  const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   // positions do not depend on the request: start their loads first
   int64_t p[kTokPerThread];
 #pragma unroll
@@ -80,24 +92,37 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  // phase 1: table index of every token of the thread (-1: PAD without lookup)
+  int64_t idx[kTokPerThread], off[kTokPerThread];
+  int last_r = -1;
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
-    if (t >= a.max_num_tokens) break;
-    int64_t slot = kPad;
+    idx[k] = -1;
+    off[k] = 0;
     if (t < a.num_tokens) {
-      const int r = request_of(q, a.num_reqs, t);
+      const int r = request_of_cached(q, a.num_reqs, t, last_r);
       if (r >= 0) {
         if (p[k] < 0) {
           err |= KV_ERR_BAD_POSITION;
         } else {
-          const int64_t lb = p[k] / a.block_size;
-          if (lb < stride)
-            slot = slot_of(table[(int64_t)r * stride + lb], p[k], a.block_size, a.num_blocks, err);
+          int64_t lb;
+          a.bs.divmod(p[k], lb, off[k]);
+          if (lb < stride) idx[k] = (int64_t)r * stride + lb;
         }
       }
     }
-    a.slot_mapping[t] = slot;
+  }
+  // phase 2: all table loads in flight together
+  int32_t blk[kTokPerThread];
+#pragma unroll
+  for (int k = 0; k < kTokPerThread; ++k) blk[k] = idx[k] >= 0 ? table[idx[k]] : kNull;
+  // phase 3: slots
+#pragma unroll
+  for (int k = 0; k < kTokPerThread; ++k) {
+    const int32_t t = base + k * kThreads;
+    if (t < a.max_num_tokens)
+      a.slot_mapping[t] = slot_of(blk[k], off[k], a.bs.size, a.num_blocks, err);
   }
   report(a.err, err);
 }
@@ -114,65 +139,92 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
 // sweep over every request, so the error word does not depend on which
 // descriptors the token loop happened to read.
 
-// Warp path: all needing lanes share request r0.  The count and the first 32
-// descriptors are requested together (`pre_s`, `pre_l`: descriptor `lane`,
-// loaded before the count is known), so the steady state costs one round trip.
+// Warp path: all needing lanes share request r0.  Chunk 0 (descriptors
+// 0..31, one per lane) arrives already scanned: `end0` is the end of lane's
+// range, `s0`/`len0` its start and length, `total0` the chunk's total.  The
+// warp keeps chunk 0 across its token groups, so a request with at most 32
+// ranges costs one descriptor load per warp for all of the warp's tokens.
+// A resolved range as a window of logical blocks [lo, hi) starting at block start.
+struct RangeWindow {
+  int r = -1;
+  int64_t lo = 0, hi = 0, start = 0;
+  __device__ __forceinline__ bool has(int rr, int64_t lb) const {
+    return rr == r && lb >= lo && lb < hi;
+  }
+};
+
+__device__ __forceinline__ void range_search_chunk(int64_t end, int32_t s, int32_t len,
+                                                   int64_t cum_base, int64_t total, bool need,
+                                                   int64_t lb, RangeWindow& win, bool& found) {
+  // first lane j whose range ends past lb
+  int lo = 0, hi = 31;
+#pragma unroll
+  for (int it = 0; it < 5; ++it) {
+    const int mid = (lo + hi) >> 1;
+    const int64_t v = __shfl_sync(kFull, end, mid);
+    if (lo < hi) {
+      if (v > lb) hi = mid; else lo = mid + 1;
+    }
+  }
+  const int32_t sj = __shfl_sync(kFull, s, lo);
+  const int64_t endj = __shfl_sync(kFull, end, lo);
+  const int32_t lenj = __shfl_sync(kFull, len, lo);
+  if (need && !found && lb >= cum_base && lb < cum_base + total) {
+    found = true;
+    win.lo = endj - lenj;
+    win.hi = endj;
+    win.start = sj;
+  }
+}
+
 __device__ __forceinline__ void range_lookup_warp(const int32_t* __restrict__ rs,
                                                   const int32_t* __restrict__ rl, int nr,
-                                                  int32_t pre_s, int32_t pre_l, bool need,
-                                                  int64_t lb, int64_t& b_out, bool& found) {
+                                                  int64_t end0, int32_t s0, int32_t len0,
+                                                  int64_t total0, bool need, int64_t lb,
+                                                  RangeWindow& win, bool& found) {
   const int lane = threadIdx.x & 31;
-  int64_t cum_base = 0;
-  for (int c0 = 0; c0 < nr; c0 += 32) {
+  range_search_chunk(end0, s0, len0, 0, total0, need, lb, win, found);
+  int64_t cum_base = total0;
+  for (int c0 = 32; c0 < nr && __any_sync(kFull, need && !found); c0 += 32) {
     const int i = c0 + lane;
     int32_t s = 0, len = 0;
     if (i < nr) {
-      s = c0 == 0 ? pre_s : rs[i];
-      len = max(c0 == 0 ? pre_l : rl[i], 0);
+      s = rs[i];
+      len = max(rl[i], 0);
     }
     const int64_t incl = warp_inclusive_scan<int64_t>((int64_t)len);
     const int64_t total = __shfl_sync(kFull, incl, 31);
-    const int64_t end = cum_base + incl;  // first logical block after range i
-    // first lane j whose range ends past lb
-    int lo = 0, hi = 31;
-#pragma unroll
-    for (int it = 0; it < 5; ++it) {
-      const int mid = (lo + hi) >> 1;
-      const int64_t v = __shfl_sync(kFull, end, mid);
-      if (lo < hi) {
-        if (v > lb) hi = mid; else lo = mid + 1;
-      }
-    }
-    const int32_t sj = __shfl_sync(kFull, s, lo);
-    const int64_t endj = __shfl_sync(kFull, end, lo);
-    const int32_t lenj = __shfl_sync(kFull, len, lo);
-    if (need && !found && lb < cum_base + total) {
-      found = true;
-      b_out = (int64_t)sj + (lb - (endj - lenj));
-    }
+    range_search_chunk(cum_base + incl, s, len, cum_base, total, need, lb, win, found);
     cum_base += total;
-    if (!__any_sync(kFull, need && !found)) break;
   }
 }
 
 constexpr int kLanePrefetch = 4;  // descriptors a lane requests with the count
 
+template <int kTokPerThread>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
                           const int32_t* __restrict__ range_len,
                           const int32_t* __restrict__ num_ranges, int32_t rstride,
                           bool qsl_in_smem) {
   extern __shared__ int32_t s_qsl[];
-  const int32_t base = blockIdx.x * kTile + threadIdx.x;
+  // positions staged per thread in shared memory: all loads are issued at
+  // once, and the token loop below stays rolled (one copy of its search
+  // paths keeps the instruction footprint small)
+  __shared__ int64_t s_pos[kTokPerThread][kThreads];
+  const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   const int lane = threadIdx.x & 31;
-  int64_t p[kTokPerThread];
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
-    p[k] = t < a.num_tokens ? a.positions[t] : 0;
+    s_pos[k][threadIdx.x] = t < a.num_tokens ? a.positions[t] : 0;
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  // the warp's scanned chunk 0 of request c_r (c_nr < 0: malformed row)
+  int c_r = -1, c_nr = -1;
+  int32_t c_s = 0, c_len = 0;
+  int64_t c_end = 0, c_total = 0;
 
   // descriptor-row validation, every request, grid-wide
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < a.num_reqs;
@@ -187,34 +239,54 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
     }
   }
 
-#pragma unroll
+  RangeWindow win;  // this lane's last resolved range
+  int last_r = -1;
+#pragma unroll 1
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
-    // every lane of the warp reaches the shuffles below: no early exit here
-    const int r = t < a.num_tokens ? request_of(q, a.num_reqs, t) : -1;
+    const int64_t pk = s_pos[k][threadIdx.x];
+    // every lane of the warp reaches the votes and shuffles below: no early exit
+    const int r = t < a.num_tokens ? request_of_cached(q, a.num_reqs, t, last_r) : -1;
     bool need = false;
     if (r >= 0) {
-      if (p[k] < 0) err |= KV_ERR_BAD_POSITION;
+      if (pk < 0) err |= KV_ERR_BAD_POSITION;
       else need = true;
     }
-    const int64_t lb = need ? p[k] / a.block_size : 0;
-    bool found = false;
-    int64_t b = 0;
-    const unsigned needers = __ballot_sync(kFull, need);
-    if (needers != 0u) {
-      const int r0 = __shfl_sync(kFull, r, __ffs(needers) - 1);
-      if (__all_sync(kFull, !need || r == r0)) {
+    int64_t lb = 0, off = 0;
+    if (need) a.bs.divmod(pk, lb, off);
+    // arithmetic only while the position stays inside the lane's last range
+    bool found = need && win.has(r, lb);
+    const bool miss = need && !found;
+    const unsigned missers = __ballot_sync(kFull, miss);
+    if (missers != 0u) {
+      const int r0 = __shfl_sync(kFull, r, __ffs(missers) - 1);
+      if (__all_sync(kFull, !miss || r == r0)) {
         const int32_t* rs0 = range_start + (int64_t)r0 * rstride;
         const int32_t* rl0 = range_len + (int64_t)r0 * rstride;
-        int32_t pre_s = 0, pre_l = 0;
-        if (lane < rstride) {
-          pre_s = rs0[lane];
-          pre_l = rl0[lane];
+        if (r0 != c_r) {
+          // descriptor `lane` is requested together with the count
+          int32_t pre_s = 0, pre_l = 0;
+          if (lane < rstride) {
+            pre_s = rs0[lane];
+            pre_l = rl0[lane];
+          }
+          const int nr0 = num_ranges[r0];
+          c_r = r0;
+          c_nr = (nr0 >= 0 && nr0 <= rstride) ? nr0 : -1;  // malformed: PAD (the sweep flags it)
+          c_s = lane < c_nr ? pre_s : 0;
+          c_len = lane < c_nr ? max(pre_l, 0) : 0;
+          c_end = warp_inclusive_scan<int64_t>((int64_t)c_len);
+          c_total = __shfl_sync(kFull, c_end, 31);
         }
-        const int nr0 = num_ranges[r0];
-        if (nr0 >= 0 && nr0 <= rstride)  // malformed rows: PAD (flagged by the sweep)
-          range_lookup_warp(rs0, rl0, nr0, pre_s, pre_l, need, lb, b, found);
-      } else if (need) {
+        if (c_nr >= 0) {
+          bool got = false;
+          range_lookup_warp(rs0, rl0, c_nr, c_end, c_s, c_len, c_total, miss, lb, win, got);
+          if (got) {
+            win.r = r;
+            found = true;
+          }
+        }
+      } else if (miss) {
         const int32_t* rs = range_start + (int64_t)r * rstride;
         const int32_t* rl = range_len + (int64_t)r * rstride;
         int32_t pre_s[kLanePrefetch], pre_l[kLanePrefetch];
@@ -231,7 +303,10 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
             if (!found && i < nr) {
               const int64_t len = max(pre_l[i], 0);
               if (lb < cum + len) {
-                b = (int64_t)pre_s[i] + (lb - cum);
+                win.r = r;
+                win.lo = cum;
+                win.hi = cum + len;
+                win.start = pre_s[i];
                 found = true;
               }
               cum += len;
@@ -240,7 +315,10 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
           for (int i = kLanePrefetch; !found && i < nr; ++i) {
             const int64_t len = max(rl[i], 0);
             if (lb < cum + len) {
-              b = (int64_t)rs[i] + (lb - cum);
+              win.r = r;
+              win.lo = cum;
+              win.hi = cum + len;
+              win.start = rs[i];
               found = true;
             }
             cum += len;
@@ -249,9 +327,23 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
       }
     }
     if (t < a.max_num_tokens)
-      a.slot_mapping[t] = found ? slot_of(b, p[k], a.block_size, a.num_blocks, err) : kPad;
+      a.slot_mapping[t] =
+          found ? slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err) : kPad;
   }
   report(a.err, err);
+}
+
+// Tokens per thread: the smallest of 4, 8, 16 that keeps the grid within
+// about one wave (4 resident CTAs per SM).
+int tokens_per_thread(int32_t max_num_tokens) {
+  const int64_t wave = (int64_t)sm_count() * 4;
+  for (int tpt = 4; tpt < 16; tpt *= 2)
+    if (((int64_t)max_num_tokens + kThreads * tpt - 1) / (kThreads * tpt) <= wave) return tpt;
+  return 16;
+}
+
+int grid_for(int32_t max_num_tokens, int tpt) {
+  return max(1, (int)(((int64_t)max_num_tokens + kThreads * tpt - 1) / (kThreads * tpt)));
 }
 
 int check_common(const int32_t* qsl, const int64_t* positions, int32_t num_reqs,
@@ -287,13 +379,19 @@ extern "C" int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64
     return KV_EINVAL;
   if (d_err != nullptr && !aligned(d_err, 4)) return KV_EINVAL;
   if (max_num_tokens == 0 && num_reqs == 0) return KV_OK;
-  const int grid = max(1, (max_num_tokens + kTile - 1) / kTile);
+  const int tpt = tokens_per_thread(max_num_tokens);
+  const int grid = grid_for(max_num_tokens, tpt);
   const bool staged = num_reqs + 1 <= kQslSmemMax;
   const size_t smem = staged && num_reqs > 0 ? sizeof(int32_t) * (num_reqs + 1) : 0;
-  SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens, block_size,
-             num_blocks, slot_mapping, d_err};
-  slot_mapping_paged_kernel<<<grid, kThreads, smem, stream>>>(a, block_table, table_stride,
-                                                              staged && num_reqs > 0);
+  SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens,
+             BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
+  const bool st = staged && num_reqs > 0;
+  if (tpt == 4)
+    slot_mapping_paged_kernel<4><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
+  else if (tpt == 8)
+    slot_mapping_paged_kernel<8><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
+  else
+    slot_mapping_paged_kernel<16><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
   return launch_status();
 }
 
@@ -317,12 +415,19 @@ extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64
   }
   if (d_err != nullptr && !aligned(d_err, 4)) return KV_EINVAL;
   if (max_num_tokens == 0 && num_reqs == 0) return KV_OK;
-  const int grid = max(1, (max_num_tokens + kTile - 1) / kTile);
+  // the range kernel's per-token state is larger: at most 8 tokens per thread
+  const int tpt = min(8, tokens_per_thread(max_num_tokens));
+  const int grid = grid_for(max_num_tokens, tpt);
   const bool staged = num_reqs + 1 <= kQslSmemMax;
   const size_t smem = staged && num_reqs > 0 ? sizeof(int32_t) * (num_reqs + 1) : 0;
-  SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens, block_size,
-             num_blocks, slot_mapping, d_err};
-  slot_mapping_range_kernel<<<grid, kThreads, smem, stream>>>(
-      a, range_start, range_len, num_ranges, range_stride, staged && num_reqs > 0);
+  SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens,
+             BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
+  const bool st = staged && num_reqs > 0;
+  if (tpt == 4)
+    slot_mapping_range_kernel<4><<<grid, kThreads, smem, stream>>>(
+        a, range_start, range_len, num_ranges, range_stride, st);
+  else
+    slot_mapping_range_kernel<8><<<grid, kThreads, smem, stream>>>(
+        a, range_start, range_len, num_ranges, range_stride, st);
   return launch_status();
 }

@@ -22,6 +22,9 @@ __all__ = [
     "kv_cache_write",
     "kv_cache_gather",
     "kv_expand_kernel_blocks",
+    "kv_table_from_ranges",
+    "kv_cache_gather_range",
+    "kv_copy_blocks",
     "new_error_word",
 ]
 
@@ -228,3 +231,93 @@ def kv_expand_kernel_blocks(mgr_table: torch.Tensor, mgr_block_size: int,
         _ptr(mgr_table), R, Ms, int(mgr_block_size), int(kernel_block_size), _ptr(kernel_table),
         kernel_table.shape[1], _err_ptr(err, dev), _stream(dev)))
     return kernel_table
+
+
+def kv_table_from_ranges(range_start: torch.Tensor, range_len: torch.Tensor,
+                         num_ranges: torch.Tensor, table_stride: Optional[int] = None,
+                         block_table: Optional[torch.Tensor] = None,
+                         err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Block table int32 [num_reqs, table_stride] expanded from range descriptors."""
+    dev = range_start.device
+    for name, t in (("range_start", range_start), ("range_len", range_len),
+                    ("num_ranges", num_ranges)):
+        _need(t, name, torch.int32, dev)
+    if range_start.dim() != 2 or range_len.shape != range_start.shape:
+        raise ValueError("range_start/range_len must both be [num_reqs, range_stride]")
+    R = range_start.shape[0]
+    if num_ranges.numel() < R:
+        raise ValueError("num_ranges has fewer entries than descriptor rows")
+    if block_table is None:
+        if table_stride is None:
+            raise ValueError("give table_stride or block_table")
+        block_table = torch.empty((R, int(table_stride)), dtype=torch.int32, device=dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    if block_table.dim() != 2 or block_table.shape[0] != R:
+        raise ValueError("block_table must be [num_reqs, table_stride]")
+    lib = load()
+    check("kv_table_from_ranges", lib.kv_table_from_ranges(
+        _ptr(range_start), _ptr(range_len), _ptr(num_ranges), range_start.shape[1], R,
+        _ptr(block_table), block_table.shape[1], _err_ptr(err, dev), _stream(dev)))
+    return block_table
+
+
+def kv_cache_gather_range(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          range_start: torch.Tensor, range_len: torch.Tensor,
+                          num_ranges: torch.Tensor, gather_start: torch.Tensor,
+                          gather_end: torch.Tensor, layer: int = 0,
+                          k_out: Optional[torch.Tensor] = None,
+                          v_out: Optional[torch.Tensor] = None, out_rows: Optional[int] = None,
+                          err: Optional[torch.Tensor] = None
+                          ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """kv_cache_gather with the blocks found from range descriptors."""
+    dev = k_cache.device
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    for name, t in (("range_start", range_start), ("range_len", range_len),
+                    ("num_ranges", num_ranges), ("gather_start", gather_start),
+                    ("gather_end", gather_end)):
+        _need(t, name, torch.int32, dev)
+    L, B, T, H, D = _cache_dims(k_cache)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if range_start.dim() != 2 or range_len.shape != range_start.shape:
+        raise ValueError("range_start/range_len must both be [num_reqs, range_stride]")
+    R = gather_start.numel()
+    if gather_end.numel() != R or range_start.shape[0] < R or num_ranges.numel() < R:
+        raise ValueError("gather spans and descriptor rows disagree")
+    if k_out is None:
+        if out_rows is None:
+            out_rows = int((gather_end.long() - gather_start.long()).clamp_min(0).sum().item())
+        k_out = torch.empty((out_rows, H, D), dtype=torch.bfloat16, device=dev)
+        v_out = torch.empty((out_rows, H, D), dtype=torch.bfloat16, device=dev)
+    _need(k_out, "k_out", torch.bfloat16, dev)
+    _need(v_out, "v_out", torch.bfloat16, dev)
+    rows = k_out.shape[0] if out_rows is None else int(out_rows)
+    for t in (k_out, v_out):
+        if t.dim() < 1 or t.shape[0] < rows or t.numel() < rows * H * D:
+            raise ValueError("outputs are smaller than out_rows rows of kv_heads x head_dim")
+    lib = load()
+    check("kv_cache_gather_range", lib.kv_cache_gather_range(
+        _ptr(k_cache), _ptr(v_cache), int(layer), L, B, T, H, D, _ptr(range_start),
+        _ptr(range_len), _ptr(num_ranges), range_start.shape[1], _ptr(gather_start),
+        _ptr(gather_end), R, _ptr(k_out), _ptr(v_out), rows, _err_ptr(err, dev), _stream(dev)))
+    return k_out, v_out
+
+
+def kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor,
+                   dst_blocks: torch.Tensor, err: Optional[torch.Tensor] = None) -> None:
+    """Copy whole blocks src -> dst (every layer, K and V) in place."""
+    dev = k_cache.device
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(src_blocks, "src_blocks", torch.int32, dev)
+    _need(dst_blocks, "dst_blocks", torch.int32, dev)
+    L, B, T, H, D = _cache_dims(k_cache)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    lib = load()
+    check("kv_copy_blocks", lib.kv_copy_blocks(
+        _ptr(k_cache), _ptr(v_cache), L, B, T, H, D, _ptr(src_blocks), _ptr(dst_blocks),
+        src_blocks.numel(), _err_ptr(err, dev), _stream(dev)))

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 1
+    assert lib.kv_abi_version() == 2
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -108,3 +108,23 @@ def test_binding_refuses_cpu_tensors():
     kc = torch.zeros((1, 4, 16, 8, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         kv.kv_cache_gather(kc, kc, t, q[:1], q[:1])
+
+
+def test_next_step_calls_reject_bad_arguments(lib):
+    # kv_table_from_ranges
+    assert lib.kv_table_from_ranges(N, N, N, 257, 1, N, 8, N, N) == -2
+    assert lib.kv_table_from_ranges(N, N, N, 4, -1, N, 8, N, N) == -1
+    assert lib.kv_table_from_ranges(N, N, N, 4, 1, N, 8, N, N) == -1  # num_ranges NULL
+    assert lib.kv_table_from_ranges(N, N, N, 4, 0, N, 8, N, N) == 0
+    # kv_cache_gather_range
+    assert lib.kv_cache_gather_range(0x1000, 0x2000, 0, 1, 8, 16, 8, 64, N, N, N, 257, 0x3000,
+                                     0x4000, 1, N, N, 0, N, N) == -2
+    assert lib.kv_cache_gather_range(0x1000, 0x2000, 0, 1, 8, 16, 8, 64, N, N, N, 4, 0x3000,
+                                     0x4000, 2, N, N, 0, N, N) == -1  # num_ranges NULL
+    assert lib.kv_cache_gather_range(0x1000, 0x2000, 2, 1, 8, 16, 8, 64, N, N, N, 4, N, N, 0, N,
+                                     N, 0, N, N) == -1  # layer out of range
+    # kv_copy_blocks
+    assert lib.kv_copy_blocks(N, N, 1, 8, 16, 3, 5, N, N, 1, N, N) == -2
+    assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 1, N, N) == -1
+    assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 0, N, N) == 0
+    assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, -1, N, N) == -1

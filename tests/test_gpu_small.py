@@ -347,3 +347,27 @@ def test_expand_random_parity(k, extra):
                                                              device=dev()), err=e)
     assert int(e.item()) == exp_e
     assert np.array_equal(out.cpu().numpy(), exp)
+
+
+@pytest.mark.parametrize("n_max", [1000, 700_000, 1_300_000, 2_600_000])
+def test_slot_mapping_tile_variants(n_max):
+    """Large batches switch to 8 and 16 tokens per thread; results are unchanged."""
+    rng = np.random.default_rng(n_max)
+    T, R = 16, 37
+    lens = rng.multinomial(n_max - 5, np.ones(R) / R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    stride = wl.table_stride_for(int(lens.max()) // T + 2, T)
+    B = R * stride + 1
+    table = rng.permutation(np.arange(1, B)).astype(np.int32)[:R * stride].reshape(R, stride)
+    pos = np.concatenate([np.arange(n, dtype=np.int64) for n in lens])
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
+    s, e = run_paged(q, pos, table, N, n_max, T, B)
+    assert e == exp_e == 0 and np.array_equal(s, exp_s)
+    # the same layout as one range per table row
+    rs = table[:, :1].copy()
+    rl = np.ones((R, 1), np.int32)
+    nr = np.ones(R, np.int32)
+    exp_r, exp_re = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    sr, er = run_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    assert er == exp_re and np.array_equal(sr, exp_r)
