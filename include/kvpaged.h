@@ -1,8 +1,9 @@
 /*
  * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
  *
- * Eight calls, each one kernel launch on the caller's stream:
+ * Nine calls, each one kernel launch on the caller's stream:
  *   kv_slot_mapping_paged    token -> cache slot through a block table
+ *   kv_slot_mapping_paged_cp the same, for one rank of context parallelism
  *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
  *   kv_cache_write           scatter new K/V rows into the paged caches
  *   kv_cache_gather          gather a request's K/V through its block table
@@ -113,6 +114,37 @@ int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64_t* positio
                           int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
                           int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
                           kv_stream_t stream);
+
+/*
+ * kv_slot_mapping_paged_cp -- kv_slot_mapping_paged filtered for one rank of
+ * decode/prefill context parallelism.
+ *
+ * [BT] Entwurfsmotivation: with TOTAL_CP_WORLD_SIZE, TOTAL_CP_RANK and
+ * CP_KV_CACHE_INTERLEAVE_SIZE the slot-mapping kernel writes real slots only
+ * for the tokens of its own rank and PAD for all others; [VBM] Symbol Map:
+ * DCP multiplies the block size of attention groups.  The pages stop before
+ * the formula; this library's reading (its parity is pinned only at world
+ * size 1 and by the partition properties): a table entry b names a virtual
+ * block of block_size * W tokens, dealt to the W ranks in chunks of I tokens,
+ * round robin; position p belongs to rank (p / I) % W and, on that rank, is
+ * element ((p % (block_size*W)) / (I*W)) * I + p % I of physical block b, so
+ * its slot is b * block_size + that element.  Each rank thus holds
+ * block_size tokens of every virtual block, every token lives on exactly one
+ * rank, and W = 1 gives kv_slot_mapping_paged.  All other rules (PAD, null
+ * entries, errors, tail) are those of kv_slot_mapping_paged, with the table
+ * indexed by p / (block_size * W).
+ *
+ *   cp_world_size W >= 1, 0 <= cp_rank < W, cp_interleave I >= 1.
+ * Errors: as kv_slot_mapping_paged; KV_EINVAL for the ranges above or
+ * block_size * W beyond int32; KV_EUNSUPPORTED when I does not divide
+ * block_size.
+ */
+int kv_slot_mapping_paged_cp(const int32_t* query_start_loc, const int64_t* positions,
+                             const int32_t* block_table, int32_t table_stride, int32_t num_reqs,
+                             int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
+                             int64_t num_blocks, int32_t cp_world_size, int32_t cp_rank,
+                             int32_t cp_interleave, int64_t* slot_mapping, int32_t* d_err,
+                             kv_stream_t stream);
 
 /*
  * kv_slot_mapping_range -- per-token cache slot through contiguous ranges.

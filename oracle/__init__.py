@@ -51,6 +51,8 @@ def _load():
     sigs = {
         "orc_coord": ([_I64, _I64, _I64, _I64, _I64], _I64),
         "orc_slot_mapping_paged": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P], ctypes.c_int),
+        "orc_slot_mapping_paged_cp": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _I32, _I32,
+                                       _I32, _P, _P], ctypes.c_int),
         "orc_slot_mapping_range": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P],
                                    ctypes.c_int),
         "orc_table_from_ranges": ([_P, _P, _P, _I32, _I32, _I32, _P, _P], ctypes.c_int),
@@ -109,6 +111,23 @@ def slot_mapping_paged(qsl, positions, block_table, num_tokens: int, max_num_tok
     _check(_load().orc_slot_mapping_paged(_ptr(qsl), _ptr(positions), _ptr(table), table.shape[1], R,
                                           num_tokens, max_num_tokens, block_size, num_blocks,
                                           _ptr(out), _ptr(err)))
+    return out, int(err[0])
+
+
+def slot_mapping_paged_cp(qsl, positions, block_table, num_tokens: int, max_num_tokens: int,
+                          block_size: int, num_blocks: int, cp_world_size: int, cp_rank: int,
+                          cp_interleave: int) -> Tuple[np.ndarray, int]:
+    """Context-parallel paged slot mapping (parity unpinned beyond world size 1)."""
+    qsl = _c(qsl, np.int32)
+    positions = _c(positions, np.int64)
+    table = _c(block_table, np.int32)
+    R = len(qsl) - 1
+    out = np.empty(max_num_tokens, dtype=np.int64)
+    err = np.zeros(1, dtype=np.int32)
+    _check(_load().orc_slot_mapping_paged_cp(_ptr(qsl), _ptr(positions), _ptr(table),
+                                             table.shape[1], R, num_tokens, max_num_tokens,
+                                             block_size, num_blocks, cp_world_size, cp_rank,
+                                             cp_interleave, _ptr(out), _ptr(err)))
     return out, int(err[0])
 
 

@@ -123,6 +123,62 @@ int orc_slot_mapping_paged(const int32_t* qsl, const int64_t* positions,
 }
 
 /* --------------------------------------------------------------------- */
+/* Context-parallel filter of the paged slot mapping.  PARITY UNPINNED beyond
+ * world size 1: [BT] Entwurfsmotivation names the three constants
+ * (TOTAL_CP_WORLD_SIZE, TOTAL_CP_RANK, CP_KV_CACHE_INTERLEAVE_SIZE) and says
+ * the kernel writes real slots only for the tokens of its own rank, PAD for
+ * all others; [VBM] Symbol Map says DCP multiplies the block size of
+ * attention groups; [BT] Grenzen und Fehler falls back to world size 1.  The
+ * formula itself is cut off with the listing.  READING: a table entry names a
+ * virtual block of block_size * W tokens; its tokens are dealt to the ranks
+ * in interleave chunks of I tokens, round robin, so position p belongs to
+ * rank (p / I) % W; on its rank, token p is element
+ * ((p % (T*W)) / (I*W)) * I + p % I of the rank's physical block b, whose
+ * slot is b * T + that element (T = block_size, T % I == 0).  With W = 1 this
+ * is orc_slot_mapping_paged.                                                */
+static int64_t paged_cp_slot(int64_t p, const int32_t* row, int32_t stride, int32_t T,
+                             int64_t B, int32_t W, int32_t rank, int32_t I, int32_t* err)
+{
+    if (p < 0) { *err |= ORC_BAD_POSITION; return ORC_PAD_SLOT; }
+    int64_t virt = (int64_t)T * W;
+    if ((p / I) % W != rank) return ORC_PAD_SLOT;
+    int64_t lb = p / virt;
+    if (lb >= stride) return ORC_PAD_SLOT;
+    int64_t b = row[lb];
+    if (b == ORC_NULL_BLOCK) return ORC_PAD_SLOT;
+    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }
+    int64_t v = p % virt;
+    return b * T + (v / ((int64_t)I * W)) * I + p % I;
+}
+
+int orc_slot_mapping_paged_cp(const int32_t* qsl, const int64_t* positions,
+                              const int32_t* block_table, int32_t table_stride,
+                              int32_t num_reqs, int32_t num_tokens, int32_t max_num_tokens,
+                              int32_t block_size, int64_t num_blocks, int32_t cp_world_size,
+                              int32_t cp_rank, int32_t cp_interleave, int64_t* slot_mapping,
+                              int32_t* err)
+{
+    if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens || block_size <= 0 ||
+        num_blocks < 1 || table_stride < 0 || cp_world_size < 1 || cp_rank < 0 ||
+        cp_rank >= cp_world_size || cp_interleave < 1)
+        return ORC_EINVAL;
+    if (block_size % cp_interleave != 0) return ORC_EUNSUPPORTED;
+    int32_t e = 0;
+    for (int32_t t = 0; t < max_num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;
+    e |= qsl_errors(qsl, num_reqs, num_tokens);
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        int32_t lo = qsl[r] < 0 ? 0 : qsl[r];
+        int32_t hi = qsl[r + 1] > num_tokens ? num_tokens : qsl[r + 1];
+        const int32_t* row = block_table + (int64_t)r * table_stride;
+        for (int32_t t = lo; t < hi; ++t)
+            slot_mapping[t] = paged_cp_slot(positions[t], row, table_stride, block_size,
+                                            num_blocks, cp_world_size, cp_rank, cp_interleave, &e);
+    }
+    *err |= e;
+    return ORC_OK;
+}
+
+/* --------------------------------------------------------------------- */
 /* Range descriptors: [RNG] The Innovation,
  *   physical_block = range_start + (position // block_size - range_cum),
  * where range_cum is the number of logical blocks the request's earlier

@@ -35,6 +35,8 @@ _I64 = ctypes.c_int64
 SIGNATURES = {
     "kv_slot_mapping_paged": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P],
                               ctypes.c_int),
+    "kv_slot_mapping_paged_cp": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _I32, _I32, _I32,
+                                  _P, _P, _P], ctypes.c_int),
     "kv_slot_mapping_range": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P],
                               ctypes.c_int),
     "kv_cache_write": ([_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _P],

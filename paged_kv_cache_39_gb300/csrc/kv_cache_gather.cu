@@ -243,16 +243,8 @@ cache_gather_range_kernel(GatherArgs a, const int32_t* __restrict__ range_start,
   uint32_t err = 0;
   // descriptor-row validation, every request, grid-wide
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < a.num_reqs;
-       r += gridDim.x * blockDim.x) {
-    const int n = num_ranges[r];
-    if (n < 0 || n > rstride) {
-      err |= KV_ERR_BAD_RANGE;
-    } else {
-      const int32_t* l_ = range_len + (int64_t)r * rstride;
-      for (int i = 0; i < n; ++i)
-        if (l_[i] <= 0) { err |= KV_ERR_BAD_RANGE; break; }
-    }
-  }
+       r += gridDim.x * blockDim.x)
+    if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
   const int64_t total = packed_offsets(a, s_off, s_start, s_warp_sum, err);
   const int64_t rows = total < a.out_rows ? total : a.out_rows;
   RangeResolver res{range_start, range_len, num_ranges, rstride};

@@ -95,6 +95,26 @@ __device__ __forceinline__ int find_span64(const int64_t* q, int n, int64_t t) {
   return lo - 1;
 }
 
+// True when descriptor row r is malformed: its count lies outside
+// [0, stride] or one of its first `count` lengths is <= 0.  The count and the
+// first four lengths are requested together (one round trip for the usual
+// short rows).
+__device__ __forceinline__ bool range_row_malformed(const int32_t* __restrict__ num_ranges,
+                                                    const int32_t* __restrict__ range_len,
+                                                    int r, int32_t stride) {
+  const int32_t* rl = range_len + (int64_t)r * stride;
+  int32_t l4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) l4[i] = i < stride ? rl[i] : 1;
+  const int n = num_ranges[r];
+  if (n < 0 || n > stride) return true;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bad |= (i < n && l4[i] <= 0);
+  for (int i = 4; i < n && !bad; ++i) bad = rl[i] <= 0;
+  return bad;
+}
+
 template <typename T>
 __device__ __forceinline__ T warp_inclusive_scan(T v) {
   const int lane = threadIdx.x & 31;

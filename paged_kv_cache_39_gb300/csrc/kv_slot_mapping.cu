@@ -77,10 +77,22 @@ __device__ __forceinline__ int64_t slot_of(int64_t b, int64_t off, int32_t T, in
   return b * T + off;
 }
 
-template <int kTokPerThread>
+// Context-parallel filter: a table entry names a virtual block of T * W
+// tokens dealt to the W ranks in chunks of I tokens, round robin; this rank
+// keeps its own tokens (element ((p % (T*W)) / (I*W)) * I + p % I of its
+// physical block) and pads the others.  W = 1 is the plain paged map.
+struct CpArgs {
+  int32_t world, rank;
+  BlockDiv chunk;   // I
+  BlockDiv ranks;   // W
+  BlockDiv virt;    // T * W
+  BlockDiv stripe;  // I * W
+};
+
+template <int kTokPerThread, bool kCP>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t stride,
-                          bool qsl_in_smem) {
+                          bool qsl_in_smem, CpArgs cp) {
   extern __shared__ int32_t s_qsl[];
   const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   // positions do not depend on the request: start their loads first
@@ -105,6 +117,16 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
       if (r >= 0) {
         if (p[k] < 0) {
           err |= KV_ERR_BAD_POSITION;
+        } else if (kCP) {
+          int64_t c, in_chunk, owner_q, owner, lb, v, stripe, unused;
+          cp.chunk.divmod(p[k], c, in_chunk);
+          cp.ranks.divmod(c, owner_q, owner);
+          if (owner == cp.rank) {
+            cp.virt.divmod(p[k], lb, v);
+            cp.stripe.divmod(v, stripe, unused);
+            off[k] = stripe * cp.chunk.size + in_chunk;
+            if (lb < stride) idx[k] = (int64_t)r * stride + lb;
+          }
         } else {
           int64_t lb;
           a.bs.divmod(p[k], lb, off[k]);
@@ -228,16 +250,8 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
 
   // descriptor-row validation, every request, grid-wide
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < a.num_reqs;
-       r += gridDim.x * blockDim.x) {
-    const int nr = num_ranges[r];
-    if (nr < 0 || nr > rstride) {
-      err |= KV_ERR_BAD_RANGE;
-    } else {
-      const int32_t* rl = range_len + (int64_t)r * rstride;
-      for (int i = 0; i < nr; ++i)
-        if (rl[i] <= 0) { err |= KV_ERR_BAD_RANGE; break; }
-    }
-  }
+       r += gridDim.x * blockDim.x)
+    if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
 
   RangeWindow win;  // this lane's last resolved range
   int last_r = -1;
@@ -359,17 +373,12 @@ int check_common(const int32_t* qsl, const int64_t* positions, int32_t num_reqs,
   return KV_OK;
 }
 
-}  // namespace
-}  // namespace kvp
-
-using namespace kvp;
-
-extern "C" int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64_t* positions,
-                                     const int32_t* block_table, int32_t table_stride,
-                                     int32_t num_reqs, int32_t num_tokens,
-                                     int32_t max_num_tokens, int32_t block_size,
-                                     int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
-                                     kv_stream_t stream) {
+template <bool kCP>
+int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
+                 const int32_t* block_table, int32_t table_stride, int32_t num_reqs,
+                 int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
+                 int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err, kv_stream_t stream,
+                 const CpArgs& cp) {
   int rc = check_common(query_start_loc, positions, num_reqs, num_tokens, max_num_tokens,
                         block_size, num_blocks, slot_mapping);
   if (rc != KV_OK) return rc;
@@ -387,12 +396,54 @@ extern "C" int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64
              BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
   const bool st = staged && num_reqs > 0;
   if (tpt == 4)
-    slot_mapping_paged_kernel<4><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
+    slot_mapping_paged_kernel<4, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                        table_stride, st, cp);
   else if (tpt == 8)
-    slot_mapping_paged_kernel<8><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
+    slot_mapping_paged_kernel<8, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                        table_stride, st, cp);
   else
-    slot_mapping_paged_kernel<16><<<grid, kThreads, smem, stream>>>(a, block_table, table_stride, st);
+    slot_mapping_paged_kernel<16, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                         table_stride, st, cp);
   return launch_status();
+}
+
+}  // namespace
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64_t* positions,
+                                     const int32_t* block_table, int32_t table_stride,
+                                     int32_t num_reqs, int32_t num_tokens,
+                                     int32_t max_num_tokens, int32_t block_size,
+                                     int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
+                                     kv_stream_t stream) {
+  return launch_paged<false>(query_start_loc, positions, block_table, table_stride, num_reqs,
+                             num_tokens, max_num_tokens, block_size, num_blocks, slot_mapping,
+                             d_err, stream, CpArgs{});
+}
+
+extern "C" int kv_slot_mapping_paged_cp(const int32_t* query_start_loc,
+                                        const int64_t* positions, const int32_t* block_table,
+                                        int32_t table_stride, int32_t num_reqs,
+                                        int32_t num_tokens, int32_t max_num_tokens,
+                                        int32_t block_size, int64_t num_blocks,
+                                        int32_t cp_world_size, int32_t cp_rank,
+                                        int32_t cp_interleave, int64_t* slot_mapping,
+                                        int32_t* d_err, kv_stream_t stream) {
+  if (cp_world_size < 1 || cp_rank < 0 || cp_rank >= cp_world_size || cp_interleave < 1 ||
+      block_size <= 0)
+    return KV_EINVAL;
+  if (block_size % cp_interleave != 0) return KV_EUNSUPPORTED;
+  if ((int64_t)block_size * cp_world_size > INT32_MAX ||
+      (int64_t)cp_interleave * cp_world_size > INT32_MAX)
+    return KV_EINVAL;
+  const CpArgs cp{cp_world_size, cp_rank, BlockDiv::make(cp_interleave),
+                  BlockDiv::make(cp_world_size), BlockDiv::make(block_size * cp_world_size),
+                  BlockDiv::make(cp_interleave * cp_world_size)};
+  return launch_paged<true>(query_start_loc, positions, block_table, table_stride, num_reqs,
+                            num_tokens, max_num_tokens, block_size, num_blocks, slot_mapping,
+                            d_err, stream, cp);
 }
 
 extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64_t* positions,

@@ -18,6 +18,7 @@ from ._lib import check, load
 
 __all__ = [
     "kv_slot_mapping_paged",
+    "kv_slot_mapping_paged_cp",
     "kv_slot_mapping_range",
     "kv_cache_write",
     "kv_cache_gather",
@@ -96,6 +97,40 @@ def kv_slot_mapping_paged(query_start_loc: torch.Tensor, positions: torch.Tensor
         _ptr(query_start_loc), _ptr(positions), _ptr(block_table), block_table.shape[1],
         max(num_reqs, 0), n, n_max, int(block_size), int(num_blocks), _ptr(slot_mapping),
         _err_ptr(err, dev), _stream(dev)))
+    return slot_mapping
+
+
+def kv_slot_mapping_paged_cp(query_start_loc: torch.Tensor, positions: torch.Tensor,
+                             block_table: torch.Tensor, block_size: int, num_blocks: int,
+                             cp_world_size: int, cp_rank: int, cp_interleave: int = 1,
+                             max_num_tokens: Optional[int] = None,
+                             slot_mapping: Optional[torch.Tensor] = None,
+                             num_tokens: Optional[int] = None,
+                             err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """kv_slot_mapping_paged for one rank of context parallelism (see the header)."""
+    dev = positions.device
+    _need(query_start_loc, "query_start_loc", torch.int32, dev)
+    _need(positions, "positions", torch.int64, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [num_reqs, table_stride]")
+    num_reqs = query_start_loc.numel() - 1
+    if block_table.shape[0] < num_reqs:
+        raise ValueError("block_table has fewer rows than requests")
+    n = positions.numel() if num_tokens is None else int(num_tokens)
+    if n > positions.numel():
+        raise ValueError("num_tokens exceeds positions")
+    n_max = n if max_num_tokens is None else int(max_num_tokens)
+    if slot_mapping is None:
+        slot_mapping = torch.empty(n_max, dtype=torch.int64, device=dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    if slot_mapping.numel() < n_max:
+        raise ValueError("slot_mapping is shorter than max_num_tokens")
+    lib = load()
+    check("kv_slot_mapping_paged_cp", lib.kv_slot_mapping_paged_cp(
+        _ptr(query_start_loc), _ptr(positions), _ptr(block_table), block_table.shape[1],
+        max(num_reqs, 0), n, n_max, int(block_size), int(num_blocks), int(cp_world_size),
+        int(cp_rank), int(cp_interleave), _ptr(slot_mapping), _err_ptr(err, dev), _stream(dev)))
     return slot_mapping
 
 

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 2
+    assert lib.kv_abi_version() == 3
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -128,3 +128,11 @@ def test_next_step_calls_reject_bad_arguments(lib):
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 1, N, N) == -1
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 0, N, N) == 0
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, -1, N, N) == -1
+
+
+def test_cp_slot_mapping_rejects_bad_arguments(lib):
+    assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 0, 0, 1, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 2, 1, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 0, 0, N, N, N) == -1
+    assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 0, 3, N, N, N) == -2
+    assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 1, 4, N, N, N) == 0

@@ -371,3 +371,33 @@ def test_slot_mapping_tile_variants(n_max):
     exp_r, exp_re = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
     sr, er = run_range(q, pos, rs, rl, nr, N, n_max, T, B)
     assert er == exp_re and np.array_equal(sr, exp_r)
+
+
+# ------------------------------------------- context-parallel slot mapping
+
+
+@pytest.mark.parametrize("W,I,T", [(1, 1, 16), (2, 1, 16), (4, 4, 16), (8, 2, 16), (3, 2, 4),
+                                   (2, 16, 16), (4, 1, 32)])
+def test_cp_slot_mapping_parity_and_partition(W, I, T):
+    rng = np.random.default_rng(12000 + W * 100 + I * 10 + T)
+    R, stride = 6, 32
+    B = 400
+    table = rng.integers(-1, B + 2, size=(R, stride)).astype(np.int32)
+    table[rng.random(table.shape) < 0.1] = 0
+    lens = rng.integers(0, 300, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    pos = rng.integers(-1, stride * T * W + 50, size=N).astype(np.int64)
+    owned = np.zeros(N, np.int64)
+    for k in range(W):
+        exp_s, exp_e = oracle.slot_mapping_paged_cp(q, pos, table, N, N + 9, T, B, W, k, I)
+        e = err_word()
+        s = kv.kv_slot_mapping_paged_cp(cuda(q), cuda(pos), cuda(table), T, B, W, k, I,
+                                        max_num_tokens=N + 9, err=e)
+        got = s.cpu().numpy()
+        assert int(e.item()) == exp_e
+        assert np.array_equal(got, exp_s)
+        owned += got[:N] >= 0
+    # every token with a valid table entry lives on exactly one rank
+    ref, _ = oracle.slot_mapping_paged_cp(q, pos, table, N, N, T * W, B, 1, 0, 1)
+    assert np.array_equal(owned, (ref >= 0).astype(np.int64))

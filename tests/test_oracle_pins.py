@@ -256,6 +256,68 @@ def test_paged_slots_unique_and_in_owned_blocks():
             assert real[t] % w.block_size == w.positions[t] % w.block_size
 
 
+# ------------------------------------- context-parallel filter (unpinned)
+# The filter's formula is not on the pages (the listing is cut off): only the
+# world-size-1 case and the stated properties (real slots for the rank's own
+# tokens, PAD elsewhere; every token on exactly one rank) are pinned.
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_cp_world_size_one_is_the_paged_map(seed):
+    rng = _rng(800 + seed)
+    T = int(rng.choice([4, 16]))
+    table = rng.integers(-1, 40, size=(3, 8)).astype(np.int32)
+    lens = rng.integers(0, 30, size=3)
+    qsl = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(qsl[-1])
+    pos = rng.integers(-1, 9 * T, size=N).astype(np.int64)
+    a, ea = oracle.slot_mapping_paged(qsl, pos, table, N, N + 3, T, 40)
+    for I in (1, 2, T):
+        b, eb = oracle.slot_mapping_paged_cp(qsl, pos, table, N, N + 3, T, 40, 1, 0, I)
+        assert eb == ea and np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("W,I,T", [(2, 1, 16), (4, 1, 16), (4, 4, 16), (8, 2, 16), (2, 16, 16),
+                                   (3, 2, 4)])
+def test_cp_partition_and_balance(W, I, T):
+    rng = _rng(900 + W * 10 + I)
+    stride = 6
+    table = rng.permutation(np.arange(1, 100))[:2 * stride].reshape(2, stride).astype(np.int32)
+    n = stride * T * W
+    qsl = np.array([0, n, 2 * n], np.int32)
+    pos = np.concatenate([np.arange(n), np.arange(n)]).astype(np.int64)
+    per_rank = []
+    for k in range(W):
+        s_, e_ = oracle.slot_mapping_paged_cp(qsl, pos, table, 2 * n, 2 * n, T, 100, W, k, I)
+        assert e_ == 0
+        per_rank.append(s_)
+    owned = np.stack([s_ >= 0 for s_ in per_rank])
+    assert (owned.sum(axis=0) == 1).all()          # every token on exactly one rank
+    for k, s_ in enumerate(per_rank):
+        mine = s_[s_ >= 0]
+        assert len(np.unique(mine)) == len(mine)    # distinct slots per rank
+        t_idx = np.nonzero(s_ >= 0)[0]
+        r_idx = (t_idx >= n).astype(int)
+        lb = pos[t_idx] // (T * W)
+        assert np.array_equal(mine // T, table[r_idx, lb])   # in the entry's block
+        # balance: each virtual block gives each rank exactly T tokens, offsets 0..T-1
+        for r in range(2):
+            for j in range(stride):
+                sel = (r_idx == r) & (lb == j)
+                assert sorted((mine[sel] % T).tolist()) == list(range(T))
+
+
+def test_cp_rejects_bad_arguments():
+    args = ([0, 1], [0], np.array([[1]], np.int32), 1, 1, 16, 4)
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.slot_mapping_paged_cp(*args, 2, 0, 3)   # interleave does not divide block size
+    assert ei.value.status == oracle.EUNSUPPORTED
+    for W, k, I in ((0, 0, 1), (2, 2, 1), (2, -1, 1), (2, 0, 0)):
+        with pytest.raises(oracle.OracleError) as ei:
+            oracle.slot_mapping_paged_cp(*args, W, k, I)
+        assert ei.value.status == oracle.EINVAL
+
+
 # ------------------------------------------------------------ coordinates
 
 
