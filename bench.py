@@ -246,7 +246,13 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False):
     ]
     if extras:
         table2 = torch.empty_like(table)
+        slot_cp = torch.empty_like(slot_p)
         launches += [
+            Launch("slot_mapping_paged_cp[W=4,rank1]", "slot_mapping_paged_kernel",
+                   lambda: kv.kv_slot_mapping_paged_cp(qsl, pos, table, T, B, 4, 1, 1,
+                                                       max_num_tokens=n_max, slot_mapping=slot_cp,
+                                                       err=err),
+                   slotmap_bytes(N, n_max, R), N),
             Launch("table_from_ranges", "table_from_ranges_kernel",
                    lambda: kv.kv_table_from_ranges(rs, rl, nr, block_table=table2, err=err),
                    lay.table.size * 4 + int(lay.num_ranges.sum()) * 8 + R * 4, R),
