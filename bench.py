@@ -743,8 +743,32 @@ def main():
     kdist.finalize()
 
 
+def copy_ceiling(torch, dev, flush_buf, reps=10):
+    """Device-to-device copy of 1 Gi bf16 elements (read + write bytes), the
+    same copy the measured peak is taken from, timed in this run."""
+    src = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev).fill_(1)
+    dst = torch.empty_like(src)
+    dst.copy_(src)
+    times = []
+    for _ in range(reps):
+        flush_l2(flush_buf)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    best = min(times)
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"torch_copy_GBps_best": round(2 * (2 << 30) / (best * 1e-3) / 1e9, 1),
+            "torch_copy_GBps_median": round(2 * (2 << 30) / (statistics.median(times) * 1e-3) / 1e9,
+                                            1),
+            "bytes": 2 * (2 << 30)}
+
+
 def detail(torch, kv, wl, dev, args, flush_buf, stream, peak):
-    out = {}
+    out = {"copy_ceiling": copy_ceiling(torch, dev, flush_buf)}
     for name in ("decode", "mixed", "long", "hybrid"):
         b = (build_decode(torch, kv, wl, dev, extras=True) if name == "decode"
              else BUILDERS[name](torch, kv, wl, dev))
