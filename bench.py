@@ -144,7 +144,8 @@ def kernel_source_sha(kernel: str) -> str:
              "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu",
              "cache_gather_range_kernel": "kv_cache_gather.cu",
              "table_from_ranges_kernel": "kv_range_table.cu",
-             "copy_blocks_kernel": "kv_copy_blocks.cu"}
+             "copy_blocks_kernel": "kv_copy_blocks.cu",
+             "cache_gather_bulk_kernel": "kv_cache_gather.cu"}
     h = hashlib.sha256()
     for f in (files[kernel], "kv_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc", f), "rb") as fh:
@@ -256,6 +257,11 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False):
             Launch("table_from_ranges", "table_from_ranges_kernel",
                    lambda: kv.kv_table_from_ranges(rs, rl, nr, block_table=table2, err=err),
                    lay.table.size * 4 + int(lay.num_ranges.sum()) * 8 + R * 4, R),
+            Launch("cache_gather_bulk", "cache_gather_bulk_kernel",
+                   lambda: kv.kv_cache_gather(kc, vc, table, g0, g1, k_out=k_out, v_out=v_out,
+                                              out_rows=rows, err=err, bulk=True),
+                   gather_bytes(rows, rb, _touched_blocks(w.gather_start, w.gather_end, T), R),
+                   rows),
             Launch("cache_gather_range", "cache_gather_range_kernel",
                    lambda: kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, k_out=k_out,
                                                     v_out=v_out, out_rows=rows, err=err),
@@ -359,6 +365,12 @@ def build_long(torch, kv, wl, dev, small=False):
         Launch("cache_gather[G]", "cache_gather_kernel",
                lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
                                           out_rows=rows, err=err), gb, rows),
+        Launch("cache_gather_bulk[P]", "cache_gather_bulk_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tp, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err, bulk=True), gb, rows),
+        Launch("cache_gather_bulk[G]", "cache_gather_bulk_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err, bulk=True), gb, rows),
         Launch("cache_gather_range[G]", "cache_gather_range_kernel",
                lambda: kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, k_out=k_out,
                                                 v_out=v_out, out_rows=rows, err=err),

@@ -1,12 +1,13 @@
 /*
  * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
  *
- * Nine calls, each one kernel launch on the caller's stream:
+ * Ten calls, each one kernel launch on the caller's stream:
  *   kv_slot_mapping_paged    token -> cache slot through a block table
  *   kv_slot_mapping_paged_cp the same, for one rank of context parallelism
  *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
  *   kv_cache_write           scatter new K/V rows into the paged caches
  *   kv_cache_gather          gather a request's K/V through its block table
+ *   kv_cache_gather_bulk     the same gather, moved by bulk (TMA) copies
  *   kv_expand_kernel_blocks  manager-size block table -> kernel-size blocks
  *   kv_table_from_ranges     range descriptors -> block table
  *   kv_cache_gather_range    the gather, with blocks found from ranges
@@ -72,7 +73,9 @@ enum kv_error_bits {
     KV_ERR_BAD_RANGE = 8,     /* descriptor count outside [0, range_stride] or a range length <= 0 */
     KV_ERR_NULL_WRITE = 16,   /* write slot inside the null block 0 */
     KV_ERR_BAD_QSL = 32,      /* query_start_loc decreasing, negative, or past num_tokens */
-    KV_ERR_OUT_OF_SPACE = 64  /* gather rows exceed out_rows, or ranges exceed a table row */
+    KV_ERR_OUT_OF_SPACE = 64, /* gather rows exceed out_rows, or ranges exceed a table row */
+    KV_ERR_TIMEOUT = 128      /* an asynchronous bulk copy did not complete within the bounded
+                                 wait; the kernel stopped early and its output is incomplete */
 };
 
 #define KV_PAD_SLOT_ID (-1)
@@ -239,6 +242,28 @@ int kv_cache_gather(const void* k_cache, const void* v_cache, int32_t layer, int
                     const int32_t* gather_start, const int32_t* gather_end, int32_t num_reqs,
                     void* k_out, void* v_out, int64_t out_rows, int32_t* d_err,
                     kv_stream_t stream);
+
+/*
+ * kv_cache_gather_bulk -- kv_cache_gather done by the bulk-copy engine.
+ *
+ * Same arguments, output, packing, zero-row rules and error bits as
+ * kv_cache_gather.  The rows of one request inside one cache block are moved
+ * as one asynchronous bulk copy (global -> shared -> global, cp.async.bulk,
+ * at most 32 KiB per copy) issued by a single thread per CTA, two one-warp
+ * CTAs per SM: the whole-block gather with TMA bulk copies.  It reaches the
+ * same bandwidth as kv_cache_gather while occupying 64 threads per SM, which
+ * leaves the SMs to concurrent kernels.  Every wait for a copy is bounded: if
+ * one ever ran out, KV_ERR_TIMEOUT is set and that CTA's remaining rows are
+ * left unwritten.
+ * Errors: as kv_cache_gather; KV_EUNSUPPORTED for a row of more than 32 KiB
+ * (num_kv_heads * head_dim * 2 > 32768) or num_reqs > 2048.
+ */
+int kv_cache_gather_bulk(const void* k_cache, const void* v_cache, int32_t layer,
+                         int32_t num_layers, int64_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, const int32_t* block_table,
+                         int32_t table_stride, const int32_t* gather_start,
+                         const int32_t* gather_end, int32_t num_reqs, void* k_out, void* v_out,
+                         int64_t out_rows, int32_t* d_err, kv_stream_t stream);
 
 /*
  * kv_expand_kernel_blocks -- unfold manager blocks into kernel blocks.

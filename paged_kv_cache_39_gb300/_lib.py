@@ -22,6 +22,7 @@ ERR_BITS = {
     "NULL_WRITE": 16,
     "BAD_QSL": 32,
     "OUT_OF_SPACE": 64,
+    "TIMEOUT": 128,
 }
 PAD_SLOT_ID = -1
 NULL_BLOCK_ID = 0
@@ -43,6 +44,8 @@ SIGNATURES = {
                        ctypes.c_int),
     "kv_cache_gather": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P, _P,
                          _I64, _P, _P], ctypes.c_int),
+    "kv_cache_gather_bulk": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P,
+                              _P, _I64, _P, _P], ctypes.c_int),
     "kv_expand_kernel_blocks": ([_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _P], ctypes.c_int),
     "kv_table_from_ranges": ([_P, _P, _P, _I32, _I32, _P, _I32, _P, _P], ctypes.c_int),
     "kv_cache_gather_range": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P,

@@ -32,4 +32,4 @@ extern "C" const char* kv_status_string(int status) {
   }
 }
 
-extern "C" int kv_abi_version(void) { return 3; }
+extern "C" int kv_abi_version(void) { return 4; }

@@ -205,12 +205,14 @@ def kv_cache_gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: t
                     gather_start: torch.Tensor, gather_end: torch.Tensor, layer: int = 0,
                     k_out: Optional[torch.Tensor] = None, v_out: Optional[torch.Tensor] = None,
                     out_rows: Optional[int] = None,
-                    err: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    err: Optional[torch.Tensor] = None, bulk: bool = False
+                    ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Gather positions [start_r, end_r) of every request into packed [rows, H, D] buffers.
 
     ``out_rows`` (or the given outputs' row count) must be at least the total
     span length; when it is None and no outputs are given, the total is read
     back from the device spans (a synchronising convenience for tests).
+    ``bulk=True`` calls kv_cache_gather_bulk (bulk-copy engine) instead.
     """
     dev = k_cache.device
     _need(k_cache, "k_cache", torch.bfloat16, dev)
@@ -238,7 +240,8 @@ def kv_cache_gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: t
         if t.dim() < 1 or t.shape[0] < rows or t.numel() < rows * H * D:
             raise ValueError("outputs are smaller than out_rows rows of kv_heads x head_dim")
     lib = load()
-    check("kv_cache_gather", lib.kv_cache_gather(
+    name = "kv_cache_gather_bulk" if bulk else "kv_cache_gather"
+    check(name, getattr(lib, name)(
         _ptr(k_cache), _ptr(v_cache), int(layer), L, B, T, H, D, _ptr(block_table),
         block_table.shape[1], _ptr(gather_start), _ptr(gather_end), R, _ptr(k_out), _ptr(v_out),
         rows, _err_ptr(err, dev), _stream(dev)))

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 3
+    assert lib.kv_abi_version() == 4
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -136,3 +136,13 @@ def test_cp_slot_mapping_rejects_bad_arguments(lib):
     assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 0, 0, N, N, N) == -1
     assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 0, 3, N, N, N) == -2
     assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 1, 4, N, N, N) == 0
+
+
+def test_bulk_gather_rejects_unsupported_shapes(lib):
+    # rows of 40 KiB exceed a bulk stage; more than 2048 requests exceed its offsets
+    assert lib.kv_cache_gather_bulk(0x1000, 0x2000, 0, 1, 8, 16, 20, 1024, N, 0, 0x3000, 0x4000,
+                                    1, N, N, 0, N, N) == -2
+    assert lib.kv_cache_gather_bulk(0x1000, 0x2000, 0, 1, 8, 16, 8, 128, N, 0, 0x3000, 0x4000,
+                                    2049, N, N, 0, N, N) == -2
+    assert lib.kv_cache_gather_bulk(0x1000, 0x2000, 0, 1, 8, 16, 8, 128, N, 0, N, N, 0, N, N, 0,
+                                    N, N) == 0

@@ -157,6 +157,14 @@ def test_long_context_full(layout):
     src, exp_e = oracle.gather_rows(0, B, T, lay.table, w.gather_start, w.gather_end, rows)
     assert int(e.item()) == exp_e == 0
     assert device_rows_equal(k_out, kc, src, E) and device_rows_equal(v_out, vc, src, E)
+    # the bulk-copy gather gives the same bytes
+    kb, vb = torch.empty_like(k_out), torch.empty_like(v_out)
+    kv.kv_cache_gather(kc, vc, cuda(lay.table), cuda(w.gather_start), cuda(w.gather_end),
+                       k_out=kb, v_out=vb, out_rows=rows, err=e, bulk=True)
+    assert int(e.item()) == 0
+    assert torch.equal(rows_view(kb, E), rows_view(k_out, E))
+    assert torch.equal(rows_view(vb, E), rows_view(v_out, E))
+    del kb, vb
     rng = np.random.default_rng(3)
     sample = np.sort(rng.choice(rows, size=SAMPLE, replace=False))
     kflat = rows_view(kc, E)
@@ -216,6 +224,13 @@ def test_hybrid_full():
             if rows:
                 assert device_rows_equal(k_out, kc, src, E)
                 assert device_rows_equal(v_out, vc, src, E)
+                kb, vb = torch.empty_like(k_out), torch.empty_like(v_out)
+                kv.kv_cache_gather(kc, vc, kt[c:hi].contiguous(), cuda(g0), cuda(g1), k_out=kb,
+                                   v_out=vb, out_rows=rows, err=e, bulk=True)
+                assert int(e.item()) == 0
+                assert torch.equal(rows_view(kb, E), rows_view(k_out, E))
+                assert torch.equal(rows_view(vb, E), rows_view(v_out, E))
+                del kb, vb
                 sample = np.sort(rng.choice(rows, size=min(256, rows), replace=False))
                 sample_host_check(v_out, lambda n: rows_view(vc, E)[n].cpu().numpy().view(np.uint16),
                                   src, E, sample)

@@ -293,9 +293,12 @@ def test_write_nothing_to_do():
 # ------------------------------------------------------------------ gather
 
 
+@pytest.mark.parametrize("bulk", [False, True])
 @pytest.mark.parametrize("seed,R,H,D", [(0, 1, 8, 128), (1, 5, 8, 64), (2, 300, 1, 8),
                                         (3, 4096, 1, 16), (4, 17, 16, 128), (5, 9, 2, 72)])
-def test_gather_random_parity(seed, R, H, D):
+def test_gather_random_parity(seed, R, H, D, bulk):
+    if bulk and R > kv.MAX_GATHER_REQS // 2:
+        pytest.skip("the bulk gather takes at most 2048 requests")
     rng = np.random.default_rng(4000 + seed)
     T, B, L, stride = 8, 50, 2, 6
     table = rng.integers(-1, B + 2, size=(R, stride)).astype(np.int32)
@@ -314,7 +317,7 @@ def test_gather_random_parity(seed, R, H, D):
     v_out = torch.from_numpy(vo.view(np.int16).copy()).view(torch.bfloat16).to(dev())
     e = err_word()
     kv.kv_cache_gather(kc.to(dev()), vc.to(dev()), cuda(table), cuda(g0), cuda(g1), layer=layer,
-                       k_out=k_out, v_out=v_out, out_rows=out_rows, err=e)
+                       k_out=k_out, v_out=v_out, out_rows=out_rows, err=e, bulk=bulk)
     assert int(e.item()) == exp_e
     assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
 
@@ -401,3 +404,38 @@ def test_cp_slot_mapping_parity_and_partition(W, I, T):
     # every token with a valid table entry lives on exactly one rank
     ref, _ = oracle.slot_mapping_paged_cp(q, pos, table, N, N, T * W, B, 1, 0, 1)
     assert np.array_equal(owned, (ref >= 0).astype(np.int64))
+
+
+@pytest.mark.parametrize("bulk", [False, True])
+@pytest.mark.parametrize("T,H,D,R", [(16, 32, 128, 7), (32, 8, 128, 9), (16, 8, 128, 2048),
+                                     (16, 8, 128, 2049), (4, 20, 1024, 5), (16, 1, 8, 33)])
+def test_gather_chunking_and_fallback(T, H, D, R, bulk):
+    """Bulk-copy chunks of several rows per block (8 KiB rows: 4-row chunks;
+    2 KiB rows with 32-row blocks: 2 chunks per block) and the largest request
+    count it takes; rows beyond a bulk stage (40 KiB) and 2049 requests are
+    refused by the bulk gather and handled by the vector gather."""
+    rng = np.random.default_rng(13000 + T * 7 + H + D + R)
+    B, L, stride = 24, 1, 6
+    table = rng.integers(-1, B + 2, size=(R, stride)).astype(np.int32)
+    table[rng.random(table.shape) < 0.15] = 0
+    g0 = rng.integers(0, stride * T, size=R).astype(np.int32)
+    g1 = np.minimum(g0 + rng.integers(0, 3 * T, size=R), stride * T).astype(np.int32)
+    total = int((g1 - g0).sum())
+    out_rows = max(0, total - 5)
+    kc = wl.bf16_normal((L, B, T, H, D), 77)
+    vc = wl.bf16_normal((L, B, T, H, D), 78)
+    ko = np.full((out_rows, H, D), 0x2222, np.uint16)
+    vo = np.full((out_rows, H, D), 0x3333, np.uint16)
+    exp_e = oracle.cache_gather(bits(kc), bits(vc), 0, B, T, table, g0, g1, ko, vo)
+    k_out = torch.full((out_rows, H, D), 0x2222, dtype=torch.int16).view(torch.bfloat16).to(dev())
+    v_out = torch.full((out_rows, H, D), 0x3333, dtype=torch.int16).view(torch.bfloat16).to(dev())
+    e = err_word()
+    args = (kc.to(dev()), vc.to(dev()), cuda(table), cuda(g0), cuda(g1))
+    if bulk and (H * D * 2 > 32768 or R > 2048):
+        with pytest.raises(kv.KVError) as ei:
+            kv.kv_cache_gather(*args, k_out=k_out, v_out=v_out, out_rows=out_rows, err=e, bulk=True)
+        assert ei.value.status == kv.KV_EUNSUPPORTED
+        return
+    kv.kv_cache_gather(*args, k_out=k_out, v_out=v_out, out_rows=out_rows, err=e, bulk=bulk)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
