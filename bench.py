@@ -616,37 +616,65 @@ def run_reference(args, rk):
 # --------------------------------------------------------------------------
 
 def e2e_decode(torch, kv, built, steps, flush_buf, stream):
+    """The decode step through the public API from host memory: every step
+    uploads its inputs (packed in one pinned buffer, one copy), runs the four
+    calls, and reads back both slot mappings and the error word."""
     k = built.keep
     w, lay = k["w"], k["lay"]
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    host_in = {"qsl": pin(w.qsl), "pos": pin(w.positions), "table": pin(lay.table),
-               "rs": pin(lay.range_start), "rl": pin(lay.range_len), "nr": pin(lay.num_ranges),
-               "g0": pin(w.gather_start), "g1": pin(w.gather_end),
-               "key": k["key"].cpu().pin_memory(), "val": k["val"].cpu().pin_memory()}
-    host_out = {"slot_p": torch.empty_like(k["slot_p"], device="cpu").pin_memory(),
-                "slot_r": torch.empty_like(k["slot_r"], device="cpu").pin_memory(),
-                "err": torch.empty_like(k["err"], device="cpu").pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    names = ["qsl", "pos", "table", "rs", "rl", "nr", "g0", "g1", "key", "val"]
+    host_src = {"qsl": w.qsl, "pos": w.positions, "table": lay.table, "rs": lay.range_start,
+                "rl": lay.range_len, "nr": lay.num_ranges, "g0": w.gather_start,
+                "g1": w.gather_end, "key": k["key"].cpu(), "val": k["val"].cpu()}
+    # one pinned staging buffer and one device buffer, each input at a 256-byte offset
+    offs, total = {}, 0
+    for n in names:
+        offs[n] = total
+        total += -(-k[n].numel() * k[n].element_size() // 256) * 256
+    h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_stage = torch.empty(total, dtype=torch.uint8, device=k["qsl"].device)
+    dev_in = {}
+    for n in names:
+        nbytes = k[n].numel() * k[n].element_size()
+        src = host_src[n]
+        src = torch.from_numpy(np.ascontiguousarray(src)) if isinstance(src, np.ndarray) else src
+        h_stage[offs[n]:offs[n] + nbytes].copy_(src.contiguous().view(-1).view(torch.uint8))
+        dev_in[n] = d_stage[offs[n]:offs[n] + nbytes].view(k[n].dtype).view(k[n].shape)
+    # the step's calls on the uploaded inputs
+    T, B, n_max, rows = w.block_size, w.num_blocks, w.max_num_tokens, k["rows"]
+    slot_p, slot_r, err = k["slot_p"], k["slot_r"], k["err"]
+    d = dev_in
+
+    def step():
+        kv.kv_slot_mapping_paged(d["qsl"], d["pos"], d["table"], T, B, max_num_tokens=n_max,
+                                 slot_mapping=slot_p, err=err)
+        kv.kv_slot_mapping_range(d["qsl"], d["pos"], d["rs"], d["rl"], d["nr"], T, B,
+                                 max_num_tokens=n_max, slot_mapping=slot_r, err=err)
+        kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=err)
+        kv.kv_cache_gather(k["kc"], k["vc"], d["table"], d["g0"], d["g1"], k_out=k["k_out"],
+                           v_out=k["v_out"], out_rows=rows, err=err)
+
+    h_out = {"slot_p": torch.empty_like(slot_p, device="cpu").pin_memory(),
+             "slot_r": torch.empty_like(slot_r, device="cpu").pin_memory(),
+             "err": torch.empty_like(err, device="cpu").pin_memory()}
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
     times = []
     for s in range(steps):
         flush_l2(flush_buf)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for name, h in host_in.items():
-            k[name].copy_(h, non_blocking=True)
-        for l in built.launches:
-            l.fn()
-        for name, h in host_out.items():
-            h.copy_(k[name], non_blocking=True)
+        d_stage.copy_(h_stage, non_blocking=True)
+        step()
+        for n, h in h_out.items():
+            h.copy_(k[n], non_blocking=True)
         stream.synchronize()
         times.append(time.perf_counter() - t0)
     med = statistics.median(times)
     return {"value": round(built.tokens / med, 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(med * 1e3, 3),
-            "note": "median wall time of one step: pinned H2D of the step's inputs, the four "
-                    "calls, D2H of both slot mappings and the error word, stream synchronised"}
+            "note": "median wall time of one step: one pinned H2D copy of the step's packed "
+                    "inputs, the four calls, D2H of both slot mappings and the error word, "
+                    "stream synchronised"}
 
 
 # --------------------------------------------------------------------------

@@ -63,8 +63,8 @@ cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ valu
       for (int j = 0; j < kVecPerLane; ++j) {
         const int v = c0 + j * 32 + lane;
         if (v < row_vecs) {
-          kd[v] = kr[j];
-          vd[v] = vr[j];
+          st_stream(kd + v, kr[j]);
+          st_stream(vd + v, vr[j]);
         }
       }
     }
