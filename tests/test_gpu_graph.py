@@ -1,0 +1,117 @@
+"""The hot path under CUDA-graph capture.
+
+The pages pad slot mappings and tables so that a captured decode step stays
+valid while the batch changes ("Range-addressed KV cache blocks ...", The
+Innovation: stable slot-mapping values under CUDA graph capture;
+"Blocktabelle", CUDA-Graph-Padding).  Every launch here is sized by host
+arguments only, so a step captured once is replayed on new inputs written in
+place, and every replay must match the oracle bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_39_gb300 as kv
+from paged_kv_cache_39_gb300 import workloads as wl
+from gpu_helpers import bits, dev, err_word
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kv.load()
+    torch.cuda.set_device(dev())
+    yield
+    torch.cuda.synchronize()
+
+
+def _batch(seed, R_pad, n_max, T, B, stride):
+    """A padded decode batch: 1 token per live request, padding rows empty."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, R_pad + 1))
+    ctx = rng.integers(1, stride * T + 1, size=R)
+    perm = rng.permutation(np.arange(1, B))
+    table = np.zeros((R_pad, stride), np.int32)
+    k = 0
+    for r in range(R):
+        n = -(-int(ctx[r]) // T)
+        table[r, :n] = perm[k:k + n]
+        k += n
+    qsl = np.zeros(R_pad + 1, np.int32)
+    qsl[1:R + 1] = np.arange(1, R + 1)
+    qsl[R + 1:] = R
+    pos = np.zeros(n_max, np.int64)
+    pos[:R] = ctx - 1
+    g0 = np.zeros(R_pad, np.int32)
+    g1 = np.zeros(R_pad, np.int32)
+    g1[:R] = ctx
+    return R, qsl, pos, table, g0, g1
+
+
+@pytest.mark.parametrize("bulk", [False, True])
+def test_decode_step_captured_once_replayed_on_new_batches(bulk):
+    T, B, H, D, stride, R_pad = 16, 512, 8, 128, 16, 32
+    n_max = R_pad
+    out_rows = R_pad * stride * T
+    # device buffers written in place between replays
+    d_qsl = torch.zeros(R_pad + 1, dtype=torch.int32, device=dev())
+    d_pos = torch.zeros(n_max, dtype=torch.int64, device=dev())
+    d_table = torch.zeros((R_pad, stride), dtype=torch.int32, device=dev())
+    d_g0 = torch.zeros(R_pad, dtype=torch.int32, device=dev())
+    d_g1 = torch.zeros(R_pad, dtype=torch.int32, device=dev())
+    key = torch.zeros((1, n_max, H, D), dtype=torch.bfloat16, device=dev())
+    val = torch.zeros_like(key)
+    kc = wl.bf16_normal((1, B, T, H, D), 500, dev())
+    vc = wl.bf16_normal((1, B, T, H, D), 501, dev())
+    slot = torch.empty(n_max, dtype=torch.int64, device=dev())
+    k_out = torch.zeros((out_rows, H, D), dtype=torch.bfloat16, device=dev())
+    v_out = torch.zeros_like(k_out)
+    err = err_word()
+
+    def step():
+        kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
+                                 slot_mapping=slot, err=err)
+        kv.kv_cache_write(key, val, kc, vc, slot, err=err)
+        kv.kv_cache_gather(kc, vc, d_table, d_g0, d_g1, k_out=k_out, v_out=v_out,
+                           out_rows=out_rows, err=err, bulk=bulk)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    for it, seed in enumerate([11, 12, 13]):
+        R, qsl, pos, table, g0, g1 = _batch(seed, R_pad, n_max, T, B, stride)
+        new_k = wl.bf16_normal((1, n_max, H, D), 600 + it, dev())
+        new_v = wl.bf16_normal((1, n_max, H, D), 700 + it, dev())
+        kc_before, vc_before = bits(kc).copy(), bits(vc).copy()
+        d_qsl.copy_(torch.from_numpy(qsl))
+        d_pos.copy_(torch.from_numpy(pos))
+        d_table.copy_(torch.from_numpy(table))
+        d_g0.copy_(torch.from_numpy(g0))
+        d_g1.copy_(torch.from_numpy(g1))
+        key.copy_(new_k)
+        val.copy_(new_v)
+        err.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        # oracle: the same step on the host
+        exp_s, e1 = oracle.slot_mapping_paged(qsl, pos, table, R, n_max, T, B)
+        assert np.array_equal(slot.cpu().numpy(), exp_s)
+        assert (exp_s[R:] == -1).all()  # padding tokens stay PAD on every replay
+        e2 = oracle.cache_write(bits(key), bits(val), kc_before, vc_before, exp_s, B, T)
+        assert np.array_equal(bits(kc), kc_before) and np.array_equal(bits(vc), vc_before)
+        ko = np.zeros((out_rows, H, D), np.uint16)
+        vo = np.zeros((out_rows, H, D), np.uint16)
+        ko[:] = bits(k_out)  # rows past this batch's total keep earlier contents
+        vo[:] = bits(v_out)
+        e3 = oracle.cache_gather(kc_before, vc_before, 0, B, T, table, g0, g1, ko, vo)
+        assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
+        assert int(err.item()) == (e1 | e2 | e3) == 0
