@@ -577,6 +577,77 @@ def cpu_baseline(seconds):
             "host_cores": os.cpu_count()}
 
 
+def oracle_rows(seconds_cap=4.0):
+    """The oracle timed per row on bounded samples of the workloads (one host
+    core); units per second, each with its sample.  A baseline beside the GPU
+    figures, not a target."""
+    import oracle
+    from paged_kv_cache_39_gb300 import workloads as wl
+    out = {}
+
+    def timed(name, unit, n_units, sample, fn):
+        fn()  # warm
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            fn()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds_cap or reps >= 3:
+                break
+        per = el / reps
+        out[name] = {"seconds": round(per, 5), "value": round(n_units / per, 1), "unit": unit,
+                     "sample": sample}
+
+    lw = wl.long_context()
+    lp, lg = lw.layouts["P"], lw.layouts["G"]
+    T, B, N = lw.block_size, lw.num_blocks, lw.num_tokens
+    timed("slot_mapping_paged", "positions/s", N, "long context, 8 x 131072 positions, table P",
+          lambda: oracle.slot_mapping_paged(lw.qsl, lw.positions, lp.table, N, N, T, B))
+    timed("slot_mapping_range", "positions/s", N, "long context, 8 x 131072 positions, 1-16 ranges",
+          lambda: oracle.slot_mapping_range(lw.qsl, lw.positions, lg.range_start, lg.range_len,
+                                            lg.num_ranges, N, N, T, B))
+    timed("slot_mapping_paged_cp", "positions/s", N, "long context, table P, W=4 rank 1",
+          lambda: oracle.slot_mapping_paged_cp(lw.qsl, lw.positions, lp.table, N, N, T, B, 4, 1,
+                                               1))
+    timed("table_from_ranges", "entries/s", lg.table.size, "long context, 8 x 8192 entries",
+          lambda: oracle.table_from_ranges(lg.range_start, lg.range_len, lg.num_ranges,
+                                           lg.table_stride))
+    # one request's whole context (131072 rows of K and V) from a long-context cache
+    shape = (1, B, T, lw.num_kv_heads, lw.head_dim)
+    kc = np.full(shape, 0x3C01, np.uint16)
+    vc = np.full(shape, 0x3C02, np.uint16)
+    rows = 131072
+    ko = np.empty((rows, lw.num_kv_heads, lw.head_dim), np.uint16)
+    vo = np.empty_like(ko)
+    timed("cache_gather", "rows/s", rows, "long context, one request's 131072 rows (table P)",
+          lambda: oracle.cache_gather(kc, vc, 0, B, T, lp.table[:1], lw.gather_start[:1],
+                                      lw.gather_end[:1], ko, vo))
+    src, _ = oracle.gather_rows_range(0, B, T, lg.range_start[:1], lg.range_len[:1],
+                                      lg.num_ranges[:1], lw.gather_start[:1], lw.gather_end[:1],
+                                      rows)
+    timed("cache_gather_range (row resolution only)", "rows/s", rows,
+          "long context, one request's 131072 rows through its ranges (source rows only)",
+          lambda: oracle.gather_rows_range(0, B, T, lg.range_start[:1], lg.range_len[:1],
+                                           lg.num_ranges[:1], lw.gather_start[:1],
+                                           lw.gather_end[:1], rows))
+    key = np.full((1, rows, lw.num_kv_heads, lw.head_dim), 0x3C03, np.uint16)
+    slots, _ = oracle.slot_mapping_paged(lw.qsl[:2], lw.positions[:rows], lp.table[:1], rows,
+                                         rows, T, B)
+    timed("cache_write", "rows/s", rows, "long context, one request's 131072-row prefill write",
+          lambda: oracle.cache_write(key, key, kc, vc, slots, B, T))
+    perm = np.random.default_rng(5).permutation(np.arange(1, B, dtype=np.int32))
+    timed("copy_blocks", "blocks/s", 1024, "1024 block copies in a one-layer long-context cache",
+          lambda: oracle.copy_blocks(kc, vc, perm[:1024], perm[1024:2048]))
+    del kc, vc, ko, vo, key
+    h = wl.hybrid()
+    g = h.groups["full"]
+    timed("expand_kernel_blocks", "entries/s", g.mgr_table.size * 2,
+          "hybrid full-attention table 640 x 1024 -> 640 x 2048",
+          lambda: oracle.expand_kernel_blocks(g.mgr_table, 32, 16))
+    return out
+
+
 def run_reference(args, rk):
     """The oracle as the reference arm, on bounded samples of the decode step."""
     if not rk.is_main:
@@ -609,6 +680,38 @@ def run_reference(args, rk):
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def graph_decode(torch, built, steps, flush_buf):
+    """The same step captured once in a CUDA graph and replayed (how a serving
+    loop runs decode steps); L2 flushed between replays, outside the events."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for l in built.launches:
+            l.fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l in built.launches:
+            l.fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush_l2(flush_buf)
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    del g
+    return {"ms_per_step": round(ms, 4), "value": round(built.tokens / (ms * 1e-3), 1),
+            "unit": "tokens/s", "steps": steps,
+            "note": "the four calls captured once in a CUDA graph, one replay per step"}
 
 
 # --------------------------------------------------------------------------
@@ -769,6 +872,7 @@ def main():
             "paged": round(built.tokens / ((t_paged + t_write) * 1e-6), 1),
             "range": round(built.tokens / ((t_range + t_write) * 1e-6), 1)}
         line["gather_GBps"] = kernels["cache_gather"]["GB/s"]
+        line["graph"] = graph_decode(torch, built, min(args.steps, 500), flush_buf)
         line["e2e"] = e2e_decode(torch, kv, built, min(args.steps, 200), flush_buf, stream)
 
     if rk.is_main and rk.world_size == 1:
@@ -778,6 +882,8 @@ def main():
             built = None
             torch.cuda.empty_cache()
             line["configs"] = detail(torch, kv, wl, dev, args, flush_buf, stream, peak)
+            if args.cpu_seconds > 0:
+                line["oracle_rows"] = oracle_rows()
     if rk.is_main:
         print(json.dumps(line), flush=True)
     kdist.finalize()

@@ -439,3 +439,61 @@ def test_gather_chunking_and_fallback(T, H, D, R, bulk):
     kv.kv_cache_gather(*args, k_out=k_out, v_out=v_out, out_rows=out_rows, err=e, bulk=bulk)
     assert int(e.item()) == exp_e
     assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
+
+
+@pytest.mark.parametrize("T", [3, 12, 24])
+def test_non_power_of_two_block_sizes_and_huge_positions(T):
+    """Block sizes that are not powers of two take the division path, and
+    positions past 2^31 its 64-bit branch (they fall past every table row)."""
+    rng = np.random.default_rng(14000 + T)
+    R, stride, B = 9, 40, 300
+    table = rng.integers(0, B, size=(R, stride)).astype(np.int32)
+    lens = rng.integers(0, 90, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    pos = rng.integers(0, stride * T + 30, size=N).astype(np.int64)
+    big = rng.random(N) < 0.1
+    pos[big] = rng.integers(1 << 31, 1 << 33, size=int(big.sum()))
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N + 3, T, B)
+    s, e = run_paged(q, pos, table, N, N + 3, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    rs = rng.integers(1, B - 10, size=(R, 4)).astype(np.int32)
+    rl = rng.integers(1, 10, size=(R, 4)).astype(np.int32)
+    nr = rng.integers(0, 5, size=R).astype(np.int32)
+    exp_r, exp_re = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N + 3, T, B)
+    sr, er = run_range(q, pos, rs, rl, nr, N, N + 3, T, B)
+    assert er == exp_re and np.array_equal(sr, exp_r)
+    for W, I in ((2, 1), (3, T)):
+        exp_c, exp_ce = oracle.slot_mapping_paged_cp(q, pos, table, N, N + 3, T, B, W, 1, I)
+        e_ = err_word()
+        sc = kv.kv_slot_mapping_paged_cp(cuda(q), cuda(pos), cuda(table), T, B, W, 1, I,
+                                         max_num_tokens=N + 3, err=e_)
+        assert int(e_.item()) == exp_ce and np.array_equal(sc.cpu().numpy(), exp_c)
+    # write and gather with this block size
+    H, D, L = 2, 64, 2
+    live = exp_s[:N][exp_s[:N] >= 0]
+    uniq, first = np.unique(live, return_index=True)
+    slots = np.full(N, -1, np.int64)
+    idx = np.nonzero(exp_s[:N] >= 0)[0][first]
+    slots[idx] = uniq
+    key = wl.bf16_normal((L, N, H, D), 140 + T)
+    kc = wl.bf16_normal((L, B, T, H, D), 150 + T)
+    ek, ev = bits(kc).copy(), bits(kc).copy()
+    exp_we = oracle.cache_write(bits(key), bits(key), ek, ev, slots, B, T)
+    kc_d, vc_d = kc.to(dev()), kc.clone().to(dev())
+    e_ = err_word()
+    kv.kv_cache_write(key.to(dev()), key.to(dev()), kc_d, vc_d, cuda(slots), err=e_)
+    assert int(e_.item()) == exp_we
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+    g0 = rng.integers(0, stride * T // 2, size=R).astype(np.int32)
+    g1 = (g0 + rng.integers(0, stride * T // 2, size=R)).astype(np.int32)
+    rows = int((g1 - g0).sum())
+    for bulk in (False, True):
+        ko = np.zeros((rows, H, D), np.uint16)
+        vo = np.zeros((rows, H, D), np.uint16)
+        exp_ge = oracle.cache_gather(ek, ev, 1, B, T, table, g0, g1, ko, vo)
+        e_ = err_word()
+        k_out, v_out = kv.kv_cache_gather(kc_d, vc_d, cuda(table), cuda(g0), cuda(g1), layer=1,
+                                          out_rows=rows, err=e_, bulk=bulk)
+        assert int(e_.item()) == exp_ge
+        assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
