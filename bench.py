@@ -495,7 +495,8 @@ def flush_l2(buf):
 
 
 def time_steps(torch, built, steps, flush_buf, stream):
-    """Per-step and per-launch device times (ms) over `steps` steps, L2 flushed between."""
+    """Per-step and per-launch device times (ms) over `steps` steps, L2 flushed
+    between steps (launches inside a step share what the step reuses)."""
     nl = len(built.launches)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(steps)]
     for s in range(steps):
@@ -508,6 +509,22 @@ def time_steps(torch, built, steps, flush_buf, stream):
     step_ms = [evs[s][0].elapsed_time(evs[s][nl]) for s in range(steps)]
     per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)] for i in range(nl)]
     return step_ms, per
+
+
+def time_each(torch, built, reps, flush_buf, stream):
+    """Per-launch device times (ms) with the L2 flushed before every launch, so
+    no launch finds another's inputs in cache."""
+    nl = len(built.launches)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nl)] for _ in range(reps)]
+    for s in range(reps):
+        for i, l in enumerate(built.launches):
+            flush_l2(flush_buf)
+            evs[s][i][0].record(stream)
+            l.fn()
+            evs[s][i][1].record(stream)
+    torch.cuda.synchronize()
+    return [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(reps)] for i in range(nl)]
 
 
 def kernel_report(built, per, peak):
@@ -922,9 +939,10 @@ def detail(torch, kv, wl, dev, args, flush_buf, stream, peak):
             for l in b.launches:
                 l.fn()
         torch.cuda.synchronize()
-        _, per = time_steps(torch, b, args.detail_reps, flush_buf, stream)
+        per = time_each(torch, b, args.detail_reps, flush_buf, stream)
         rep = kernel_report(b, per, peak)
-        entry = {"workload": b.desc, "kernels": rep, "errors": int(b.keep["err"].item())}
+        entry = {"workload": b.desc, "kernels": rep, "errors": int(b.keep["err"].item()),
+                 "l2": "flushed before every launch", "reps": args.detail_reps}
         if name == "mixed":
             tw = rep["cache_write"]["us"]
             entry["write_slotmap_tokens_per_s"] = {

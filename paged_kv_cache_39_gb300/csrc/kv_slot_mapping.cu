@@ -89,10 +89,17 @@ struct CpArgs {
   BlockDiv stripe;  // I * W
 };
 
-template <int kTokPerThread, bool kCP>
+// Index arithmetic of the paged kernel: 64-bit in general, 32-bit when the
+// host has checked that table offsets, in-row positions and slots all fit
+// int32 (positions are 64-bit, so one 64-bit compare guards the narrowing),
+// or the context-parallel filter.
+enum class PagedMode { kWide, kNarrow, kCP };
+
+template <int kTokPerThread, PagedMode kMode>
 __global__ void __launch_bounds__(kThreads)
 slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t stride,
                           bool qsl_in_smem, CpArgs cp) {
+  constexpr bool kCP = kMode == PagedMode::kCP;
   extern __shared__ int32_t s_qsl[];
   const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   // positions do not depend on the request: start their loads first
@@ -127,6 +134,14 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
             off[k] = stripe * cp.chunk.size + in_chunk;
             if (lb < stride) idx[k] = (int64_t)r * stride + lb;
           }
+        } else if (kMode == PagedMode::kNarrow) {
+          // p < stride * T <= INT32_MAX: 32-bit block index and offset
+          if (p[k] < (int64_t)stride * a.bs.size) {
+            const uint32_t pu = (uint32_t)p[k];
+            const uint32_t lb = a.bs.shift >= 0 ? pu >> a.bs.shift : pu / (uint32_t)a.bs.size;
+            off[k] = (int32_t)(pu - lb * (uint32_t)a.bs.size);
+            idx[k] = r * stride + (int32_t)lb;
+          }
         } else {
           int64_t lb;
           a.bs.divmod(p[k], lb, off[k]);
@@ -143,8 +158,19 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
-    if (t < a.max_num_tokens)
+    if (t >= a.max_num_tokens) continue;
+    if (kMode == PagedMode::kNarrow) {
+      // num_blocks * T <= INT32_MAX: the slot of a valid block fits int32
+      const int32_t b = blk[k];
+      int64_t slot = kPad;
+      if (b != kNull) {
+        if (b < 0 || b >= a.num_blocks) err |= KV_ERR_BAD_BLOCK;
+        else slot = b * a.bs.size + (int32_t)off[k];
+      }
+      a.slot_mapping[t] = slot;
+    } else {
       a.slot_mapping[t] = slot_of(blk[k], off[k], a.bs.size, a.num_blocks, err);
+    }
   }
   report(a.err, err);
 }
@@ -373,7 +399,7 @@ int check_common(const int32_t* qsl, const int64_t* positions, int32_t num_reqs,
   return KV_OK;
 }
 
-template <bool kCP>
+template <PagedMode kMode>
 int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
                  const int32_t* block_table, int32_t table_stride, int32_t num_reqs,
                  int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
@@ -396,14 +422,14 @@ int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
              BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
   const bool st = staged && num_reqs > 0;
   if (tpt == 4)
-    slot_mapping_paged_kernel<4, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                        table_stride, st, cp);
+    slot_mapping_paged_kernel<4, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                          table_stride, st, cp);
   else if (tpt == 8)
-    slot_mapping_paged_kernel<8, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                        table_stride, st, cp);
+    slot_mapping_paged_kernel<8, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                          table_stride, st, cp);
   else
-    slot_mapping_paged_kernel<16, kCP><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                         table_stride, st, cp);
+    slot_mapping_paged_kernel<16, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
+                                                                           table_stride, st, cp);
   return launch_status();
 }
 
@@ -418,9 +444,18 @@ extern "C" int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64
                                      int32_t max_num_tokens, int32_t block_size,
                                      int64_t num_blocks, int64_t* slot_mapping, int32_t* d_err,
                                      kv_stream_t stream) {
-  return launch_paged<false>(query_start_loc, positions, block_table, table_stride, num_reqs,
-                             num_tokens, max_num_tokens, block_size, num_blocks, slot_mapping,
-                             d_err, stream, CpArgs{});
+  // 32-bit indices when every table offset, in-row position and slot fits int32
+  const bool narrow = (int64_t)num_reqs * table_stride <= INT32_MAX &&
+                      (int64_t)table_stride * block_size <= INT32_MAX &&
+                      num_blocks * (int64_t)block_size <= INT32_MAX;
+  if (narrow)
+    return launch_paged<PagedMode::kNarrow>(query_start_loc, positions, block_table,
+                                            table_stride, num_reqs, num_tokens, max_num_tokens,
+                                            block_size, num_blocks, slot_mapping, d_err, stream,
+                                            CpArgs{});
+  return launch_paged<PagedMode::kWide>(query_start_loc, positions, block_table, table_stride,
+                                        num_reqs, num_tokens, max_num_tokens, block_size,
+                                        num_blocks, slot_mapping, d_err, stream, CpArgs{});
 }
 
 extern "C" int kv_slot_mapping_paged_cp(const int32_t* query_start_loc,
@@ -441,7 +476,8 @@ extern "C" int kv_slot_mapping_paged_cp(const int32_t* query_start_loc,
   const CpArgs cp{cp_world_size, cp_rank, BlockDiv::make(cp_interleave),
                   BlockDiv::make(cp_world_size), BlockDiv::make(block_size * cp_world_size),
                   BlockDiv::make(cp_interleave * cp_world_size)};
-  return launch_paged<true>(query_start_loc, positions, block_table, table_stride, num_reqs,
+  return launch_paged<PagedMode::kCP>(query_start_loc, positions, block_table, table_stride,
+                                      num_reqs,
                             num_tokens, max_num_tokens, block_size, num_blocks, slot_mapping,
                             d_err, stream, cp);
 }

@@ -497,3 +497,32 @@ def test_non_power_of_two_block_sizes_and_huge_positions(T):
                                           out_rows=rows, err=e_, bulk=bulk)
         assert int(e_.item()) == exp_ge
         assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
+
+
+@pytest.mark.parametrize("T", [16, 24])
+def test_slot_mapping_with_slots_past_int32(T):
+    """A pool of 2^28 blocks gives slots past 2^31: the paged map takes its
+    64-bit path (the 32-bit one needs num_blocks * block_size to fit int32),
+    the range and context-parallel maps compute in 64 bits throughout."""
+    rng = np.random.default_rng(15000 + T)
+    B = 1 << 28
+    R, stride = 6, 64
+    table = rng.integers(0, B, size=(R, stride)).astype(np.int32)
+    lens = rng.integers(1, 200, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    pos = rng.integers(0, stride * T, size=N).astype(np.int64)
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N, T, B)
+    assert exp_s.max() > (1 << 31)
+    s, e = run_paged(q, pos, table, N, N, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    rs = rng.integers(1 << 27, B - 100, size=(R, 3)).astype(np.int32)
+    rl = rng.integers(1, 30, size=(R, 3)).astype(np.int32)
+    nr = np.full(R, 3, np.int32)
+    exp_r, exp_re = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+    sr, er = run_range(q, pos, rs, rl, nr, N, N, T, B)
+    assert er == exp_re and np.array_equal(sr, exp_r)
+    exp_c, exp_ce = oracle.slot_mapping_paged_cp(q, pos, table, N, N, T, B, 2, 0, 1)
+    e_ = err_word()
+    sc = kv.kv_slot_mapping_paged_cp(cuda(q), cuda(pos), cuda(table), T, B, 2, 0, 1, err=e_)
+    assert int(e_.item()) == exp_ce and np.array_equal(sc.cpu().numpy(), exp_c)
