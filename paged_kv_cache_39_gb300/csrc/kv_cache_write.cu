@@ -11,12 +11,14 @@
 // contiguous in the input and in the cache, so one warp moves one (layer,
 // token) row pair with 16-byte vector accesses: 32 lanes x 16 B = 512 B per
 // instruction, fully coalesced on both sides.  Each lane keeps up to 4 K and
-// 4 V vectors in flight (4 KiB per warp).  The slot load and the K/V loads
-// are independent, so they are issued back to back and the DRAM round trips
-// overlap.  Warps walk the (layer, token) items in a grid-stride loop over a
-// persistent grid sized to the SM count, consecutive warps taking
-// consecutive tokens of one layer (contiguous input).  Everything is 64-bit
-// addressed: a 32-layer cache passes 2^32 bytes.
+// 4 V vectors in flight (4 KiB per warp).  On large batches a warp step
+// takes 4 consecutive tokens of one layer (their slots in one load, one lane
+// each), so a warp writes the consecutive rows a prefill places in one block
+// back to back (measured +5 % over one row per step); a small batch keeps one
+// row per warp so its latency is one row's.
+// Warps walk these groups in a grid-stride loop over a persistent grid sized
+// to the SM count.  Everything is 64-bit addressed: a 32-layer cache passes
+// 2^32 bytes.
 #include "kv_common.cuh"
 
 namespace kvp {
@@ -26,6 +28,43 @@ constexpr int kThreads = 256;
 constexpr int kVecPerLane = 4;                 // 16-byte vectors per lane per chunk
 constexpr int kChunkVecs = 32 * kVecPerLane;   // 2 KiB per K (and V) chunk
 
+
+// Move one (layer, token) row pair to its slot (nothing for PAD or errors).
+__device__ __forceinline__ void write_row(const uint4* __restrict__ ks,
+                                          const uint4* __restrict__ vs, int64_t s,
+                                          int64_t layer, uint4* __restrict__ k_cache,
+                                          uint4* __restrict__ v_cache, int64_t num_blocks,
+                                          int32_t block_size, int32_t row_vecs, int lane,
+                                          uint32_t& err) {
+  for (int c0 = 0; c0 < row_vecs; c0 += kChunkVecs) {
+    uint4 kr[kVecPerLane], vr[kVecPerLane];
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+      const int v = c0 + j * 32 + lane;
+      if (v < row_vecs) {
+        kr[j] = ld_stream(ks + v);
+        vr[j] = ld_stream(vs + v);
+      }
+    }
+    if (s < 0) return;  // PAD: nothing to store (warp-uniform)
+    const int64_t b = s / block_size;
+    if (b == kNull) { err |= KV_ERR_NULL_WRITE; return; }
+    if (b >= num_blocks) { err |= KV_ERR_BAD_SLOT; return; }
+    const int64_t n = (layer * num_blocks + b) * block_size + (s - b * block_size);
+    uint4* kd = k_cache + n * row_vecs;
+    uint4* vd = v_cache + n * row_vecs;
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+      const int v = c0 + j * 32 + lane;
+      if (v < row_vecs) {
+        st_stream(kd + v, kr[j]);
+        st_stream(vd + v, vr[j]);
+      }
+    }
+  }
+}
+
+template <int kRowsPerWarp>  // consecutive tokens of one layer per warp step
 __global__ void __launch_bounds__(kThreads)
 cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -35,38 +74,20 @@ cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ valu
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t groups = (num_tokens + kRowsPerWarp - 1) / kRowsPerWarp;  // per layer
+  const int64_t units = groups * (items / num_tokens);
   uint32_t err = 0;
-  for (int64_t i = warp0; i < items; i += nwarps) {
-    const int64_t layer = i / num_tokens;
-    const int64_t t = i - layer * num_tokens;
-    const int64_t s = slot_mapping[t];
-    const uint4* ks = key + i * row_vecs;
-    const uint4* vs = value + i * row_vecs;
-    for (int c0 = 0; c0 < row_vecs; c0 += kChunkVecs) {
-      uint4 kr[kVecPerLane], vr[kVecPerLane];
-#pragma unroll
-      for (int j = 0; j < kVecPerLane; ++j) {
-        const int v = c0 + j * 32 + lane;
-        if (v < row_vecs) {
-          kr[j] = ld_stream(ks + v);
-          vr[j] = ld_stream(vs + v);
-        }
-      }
-      if (s < 0) break;  // PAD: nothing to store (warp-uniform)
-      const int64_t b = s / block_size;
-      if (b == kNull) { err |= KV_ERR_NULL_WRITE; break; }
-      if (b >= num_blocks) { err |= KV_ERR_BAD_SLOT; break; }
-      const int64_t n = (layer * num_blocks + b) * block_size + (s - b * block_size);
-      uint4* kd = k_cache + n * row_vecs;
-      uint4* vd = v_cache + n * row_vecs;
-#pragma unroll
-      for (int j = 0; j < kVecPerLane; ++j) {
-        const int v = c0 + j * 32 + lane;
-        if (v < row_vecs) {
-          st_stream(kd + v, kr[j]);
-          st_stream(vd + v, vr[j]);
-        }
-      }
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t layer = u / groups;
+    const int64_t t0 = (u - layer * groups) * kRowsPerWarp;
+    const int nt = (int)(num_tokens - t0 < kRowsPerWarp ? num_tokens - t0 : kRowsPerWarp);
+    // the slots of the group, one lane each, then shared by the warp
+    const int64_t my_s = lane < nt ? slot_mapping[t0 + lane] : -1;
+    for (int k = 0; k < nt; ++k) {
+      const int64_t s = __shfl_sync(kFull, my_s, k);
+      const int64_t i = layer * num_tokens + t0 + k;
+      write_row(key + i * row_vecs, value + i * row_vecs, s, layer, k_cache, v_cache,
+                num_blocks, block_size, row_vecs, lane, err);
     }
   }
   report(err_word, err);
@@ -97,11 +118,18 @@ extern "C" int kv_cache_write(const void* key, const void* value, void* k_cache,
       !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
     return KV_EINVAL;
   const int32_t row_vecs = (int32_t)(row_bytes / 16);
-  const int64_t warps_needed = items;
-  const int64_t ctas_needed = (warps_needed * 32 + kThreads - 1) / kThreads;
+  // Four rows per warp step once there are enough rows to keep every warp
+  // slot busy several times over; a small batch (a decode step) spreads one
+  // row per warp so that no warp serialises rows.
   const int64_t cap = (int64_t)sm_count() * (2048 / kThreads);
+  const bool grouped = items >= cap * (kThreads / 32) * 4;
+  const int rpw = grouped ? 4 : 1;
+  const int64_t warps_needed = (int64_t)num_layers * ((num_tokens + rpw - 1) / rpw);
+  const int64_t ctas_needed = (warps_needed * 32 + kThreads - 1) / kThreads;
   const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);
-  cache_write_kernel<<<grid, kThreads, 0, stream>>>(
+  auto k4 = cache_write_kernel<4>;
+  auto k1 = cache_write_kernel<1>;
+  (grouped ? k4 : k1)<<<grid, kThreads, 0, stream>>>(
       static_cast<const uint4*>(key), static_cast<const uint4*>(value),
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
       items, num_blocks, block_size, row_vecs, d_err);

@@ -526,3 +526,34 @@ def test_slot_mapping_with_slots_past_int32(T):
     e_ = err_word()
     sc = kv.kv_slot_mapping_paged_cp(cuda(q), cuda(pos), cuda(table), T, B, 2, 0, 1, err=e_)
     assert int(e_.item()) == exp_ce and np.array_equal(sc.cpu().numpy(), exp_c)
+
+
+@pytest.mark.parametrize("L,N", [(1, 40003), (3, 13333)])
+def test_write_grouped_path(L, N):
+    """Batches of tens of thousands of rows take the four-rows-per-warp write;
+    token counts not a multiple of four, PAD, null-block and bad slots included."""
+    rng = np.random.default_rng(16000 + N)
+    T, H, D = 16, 1, 64
+    B = -(-N // T) + 40
+    slots = rng.permutation(np.arange(T, B * T))[:N].astype(np.int64)
+    slots[rng.random(N) < 0.05] = -1
+    slots[rng.integers(0, N, size=7)] = rng.integers(0, T, size=7)  # null block
+    slots[rng.integers(0, N, size=5)] = B * T + 3                   # past the pool
+    # keep the valid slots unique (the write races on duplicates)
+    seen = set()
+    for i in range(N):
+        if slots[i] >= T and slots[i] < B * T:
+            if slots[i] in seen:
+                slots[i] = -1
+            seen.add(int(slots[i]))
+    key = wl.bf16_normal((L, N, H, D), 160 + L)
+    val = wl.bf16_normal((L, N, H, D), 170 + L)
+    kc = wl.bf16_normal((L, B, T, H, D), 180 + L)
+    vc = wl.bf16_normal((L, B, T, H, D), 190 + L)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_e = oracle.cache_write(bits(key), bits(val), ek, ev, slots, B, T)
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_cache_write(key.to(dev()), val.to(dev()), kc_d, vc_d, cuda(slots), err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
