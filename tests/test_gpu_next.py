@@ -176,3 +176,24 @@ def test_copy_then_write_diverges_only_the_copy():
     exp = torch.ones_like(same)
     exp[:, 3] = False
     assert torch.equal(same, exp)
+
+
+@pytest.mark.parametrize("P,L,T", [(1000, 3, 16), (2000, 4, 6)])
+def test_copy_blocks_grouped_path(P, L, T):
+    """Batches of tens of thousands of rows copy four rows per warp step; a
+    block size of 6 leaves a two-row remainder in every block."""
+    rng = np.random.default_rng(9300 + P + T)
+    H, D = 1, 32
+    B = 2 * P + 50
+    perm = rng.permutation(np.arange(1, B)).astype(np.int32)
+    src, dst = perm[:P].copy(), perm[P:2 * P].copy()
+    src[5], dst[9], src[11] = 0, 0, B + 1
+    kc = wl.bf16_normal((L, B, T, H, D), 400 + T)
+    vc = wl.bf16_normal((L, B, T, H, D), 410 + T)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_e = oracle.copy_blocks(ek, ev, src, dst)
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
