@@ -29,8 +29,21 @@ MUTANTS = [
      "    int64_t lb = p / T + 1;\n    if (lb >= stride)"),
     ("paged_null_not_skipped", "    if (b == ORC_NULL_BLOCK) return ORC_PAD_SLOT;\n    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n    return b * T + p % T;\n}\n\n/* [BT]",
      "    if (b < 0 || b >= B) { *err |= ORC_BAD_BLOCK; return ORC_PAD_SLOT; }\n    return b * T + p % T;\n}\n\n/* [BT]"),
-    ("tail_not_padded", "for (int32_t t = 0; t < max_num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n        int32_t lo",
-     "for (int32_t t = 0; t < num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n        int32_t lo"),
+    ("tail_not_padded",
+     "for (int32_t t = 0; t < max_num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n"
+     "    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n"
+     "        int32_t lo = qsl[r] < 0 ? 0 : qsl[r];\n"
+     "        int32_t hi = qsl[r + 1] > num_tokens ? num_tokens : qsl[r + 1];\n"
+     "        const int32_t* row = block_table + (int64_t)r * table_stride;\n"
+     "        for (int32_t t = lo; t < hi; ++t)\n"
+     "            slot_mapping[t] = paged_slot(",
+     "for (int32_t t = 0; t < num_tokens; ++t) slot_mapping[t] = ORC_PAD_SLOT;\n"
+     "    e |= qsl_errors(qsl, num_reqs, num_tokens);\n    for (int32_t r = 0; r < num_reqs; ++r) {\n"
+     "        int32_t lo = qsl[r] < 0 ? 0 : qsl[r];\n"
+     "        int32_t hi = qsl[r + 1] > num_tokens ? num_tokens : qsl[r + 1];\n"
+     "        const int32_t* row = block_table + (int64_t)r * table_stride;\n"
+     "        for (int32_t t = lo; t < hi; ++t)\n"
+     "            slot_mapping[t] = paged_slot("),
     ("range_sign", "int64_t b = (int64_t)rstart[i] + (lb - range_cum);",
      "int64_t b = (int64_t)rstart[i] + (lb + range_cum);"),
     ("range_cum_dropped", "            return b * T + p % T;\n        }\n        range_cum += len;",
@@ -66,6 +79,10 @@ MUTANTS = [
      "        (void)0;"),
     ("copy_direction_swapped", "k_cache[d + x] = k_cache[s + x];", "k_cache[s + x] = k_cache[d + x];"),
     ("copy_null_guard_dropped", "if (db == ORC_NULL_BLOCK) { e |= ORC_NULL_WRITE; continue; }", ""),
+    ("cp_owner_inverted", "if ((p / I) % W != rank) return ORC_PAD_SLOT;",
+     "if ((p / I) % W == rank && W > 1) return ORC_PAD_SLOT;"),
+    ("cp_local_offset_dropped_stripe", "return b * T + (v / ((int64_t)I * W)) * I + p % I;",
+     "return b * T + (v / I) + p % I;"),
     ("expand_divisor_unchecked", "if (mgr_block_size % kernel_block_size != 0) return ORC_EUNSUPPORTED;", ""),
 ]
 
