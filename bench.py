@@ -330,6 +330,10 @@ def build_long(torch, kv, wl, dev, small=False):
     rs, rl, nr = t(lg.range_start), t(lg.range_len), t(lg.num_ranges)
     g0, g1 = t(w.gather_start), t(w.gather_end)
     tg_rebuilt = torch.empty_like(tg)
+    # copy-on-write of 4096 blocks (disjoint sources and targets), 537 MB moved
+    n_cow = 4096
+    perm = np.random.default_rng(6).permutation(np.arange(1, B, dtype=np.int32))
+    cow_src, cow_dst = t(perm[:n_cow]), t(perm[n_cow:2 * n_cow])
     kc = wl.bf16_normal((1, B, T, H, D), 31, dev)
     vc = wl.bf16_normal((1, B, T, H, D), 32, dev)
     rows = w.num_tokens
@@ -378,10 +382,13 @@ def build_long(torch, kv, wl, dev, small=False):
         Launch("table_from_ranges[G]", "table_from_ranges_kernel",
                lambda: kv.kv_table_from_ranges(rs, rl, nr, block_table=tg_rebuilt, err=err),
                lg.table.size * 4 + int(lg.num_ranges.sum()) * 8 + R * 4, R),
+        Launch(f"copy_blocks[cow {n_cow}]", "copy_blocks_kernel",
+               lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err),
+               n_cow * T * w.row_bytes * 4 + n_cow * 8, n_cow),
     ]
     desc = (f"long-context gather: {R} requests x 131072 tokens, block_size 16, KV 8x128 bf16; "
             "P = permuted block table, G = 1-16 packed ranges per request; plus the prompt's "
-            "prefill write through P")
+            "prefill write through P and a 4096-block copy-on-write")
     keep = dict(kc=kc, vc=vc, k_out=k_out, v_out=v_out, key=key, val=val, err=err)
     return Built("long", desc, launches, N, keep)
 
