@@ -95,24 +95,43 @@ __device__ __forceinline__ int find_span64(const int64_t* q, int n, int64_t t) {
   return lo - 1;
 }
 
-// True when descriptor row r is malformed: its count lies outside
-// [0, stride] or one of its first `count` lengths is <= 0.  The count and the
-// first four lengths are requested together (one round trip for the usual
-// short rows).
+// Validation of descriptor row r: malformed when its count lies outside
+// [0, stride] or one of its first `count` lengths is <= 0.  load() requests
+// the count and the first four lengths together (one round trip for the
+// usual short rows) and malformed() consumes them, so a caller can issue the
+// loads early and pay for them late.
+struct RangeRowCheck {
+  int r = -1;
+  int32_t n = 0;
+  int32_t l4[4] = {1, 1, 1, 1};
+
+  __device__ __forceinline__ void load(const int32_t* __restrict__ num_ranges,
+                                       const int32_t* __restrict__ range_len, int row,
+                                       int32_t stride) {
+    r = row;
+    const int32_t* rl = range_len + (int64_t)row * stride;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l4[i] = i < stride ? rl[i] : 1;
+    n = num_ranges[row];
+  }
+  __device__ __forceinline__ bool malformed(const int32_t* __restrict__ range_len,
+                                            int32_t stride) const {
+    if (n < 0 || n > stride) return true;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bad |= (i < n && l4[i] <= 0);
+    const int32_t* rl = range_len + (int64_t)r * stride;
+    for (int i = 4; i < n && !bad; ++i) bad = rl[i] <= 0;
+    return bad;
+  }
+};
+
 __device__ __forceinline__ bool range_row_malformed(const int32_t* __restrict__ num_ranges,
                                                     const int32_t* __restrict__ range_len,
                                                     int r, int32_t stride) {
-  const int32_t* rl = range_len + (int64_t)r * stride;
-  int32_t l4[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) l4[i] = i < stride ? rl[i] : 1;
-  const int n = num_ranges[r];
-  if (n < 0 || n > stride) return true;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) bad |= (i < n && l4[i] <= 0);
-  for (int i = 4; i < n && !bad; ++i) bad = rl[i] <= 0;
-  return bad;
+  RangeRowCheck c;
+  c.load(num_ranges, range_len, r, stride);
+  return c.malformed(range_len, stride);
 }
 
 template <typename T>

@@ -262,22 +262,29 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   __shared__ int64_t s_pos[kTokPerThread][kThreads];
   const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   const int lane = threadIdx.x & 31;
+  // the position loads and the qsl staging loads are in flight together; the
+  // positions reach shared memory only after the staging barrier
+  int64_t p[kTokPerThread];
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
-    s_pos[k][threadIdx.x] = t < a.num_tokens ? a.positions[t] : 0;
+    p[k] = t < a.num_tokens ? a.positions[t] : 0;
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+#pragma unroll
+  for (int k = 0; k < kTokPerThread; ++k) s_pos[k][threadIdx.x] = p[k];
   // the warp's scanned chunk 0 of request c_r (c_nr < 0: malformed row)
   int c_r = -1, c_nr = -1;
   int32_t c_s = 0, c_len = 0;
   int64_t c_end = 0, c_total = 0;
 
-  // descriptor-row validation, every request, grid-wide
-  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < a.num_reqs;
-       r += gridDim.x * blockDim.x)
-    if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
+  // descriptor-row validation, every request, grid-wide: the thread's first
+  // row is requested now and checked after the token loop, so the check costs
+  // no round trip on the loop's critical path
+  const int sweep0 = blockIdx.x * blockDim.x + threadIdx.x;
+  RangeRowCheck first_row;
+  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, sweep0, rstride);
 
   RangeWindow win;  // this lane's last resolved range
   int last_r = -1;
@@ -369,6 +376,11 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
     if (t < a.max_num_tokens)
       a.slot_mapping[t] =
           found ? slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err) : kPad;
+  }
+  if (sweep0 < a.num_reqs) {
+    if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
+    for (int r = sweep0 + gridDim.x * blockDim.x; r < a.num_reqs; r += gridDim.x * blockDim.x)
+      if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
   }
   report(a.err, err);
 }
