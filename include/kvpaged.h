@@ -369,6 +369,19 @@ int kv_copy_blocks(void* k_cache, void* v_cache, int32_t num_layers, int64_t num
                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
                    int32_t* d_err, kv_stream_t stream);
 
+/*
+ * kv_diag_bounded_wait -- self-test of the bounded wait the bulk-copy gather
+ * relies on.  No page defines it: it exists so the timeout path can be
+ * exercised on a real GPU without faulting or hanging it.  One thread waits,
+ * for at most spin_limit tries, on a shared-memory barrier that nothing will
+ * complete; when the limit runs out it OR-s KV_ERR_TIMEOUT into *d_err and
+ * the kernel ends normally, so the context stays usable.
+ *   spin_limit  1 .. 2^20 tries.
+ *   d_err       int32 device word (required).
+ * Errors: KV_EINVAL for a limit out of range or a null/misaligned d_err.
+ */
+int kv_diag_bounded_wait(int32_t spin_limit, int32_t* d_err, kv_stream_t stream);
+
 /* Human-readable name of a kv_status value (static string). */
 const char* kv_status_string(int status);
 

@@ -22,6 +22,31 @@ int sm_count() {
 
 }  // namespace kvp
 
+namespace kvp {
+namespace {
+
+// A wait that nothing will satisfy: an mbarrier expecting one arrival that
+// never comes, waited on with the library's bounded wait.  It must give up
+// after `limit` tries and report KV_ERR_TIMEOUT, leaving the context usable.
+__global__ void bounded_wait_probe_kernel(int64_t limit, int32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  mbar_fence_init();
+  if (!mbar_wait_bounded(&bar, 0u, limit)) atomicOr(err, KV_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace kvp
+
+extern "C" int kv_diag_bounded_wait(int32_t spin_limit, int32_t* d_err, kv_stream_t stream) {
+  if (spin_limit < 1 || spin_limit > (1 << 20) || d_err == nullptr ||
+      !kvp::aligned(d_err, 4))
+    return KV_EINVAL;
+  kvp::bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(spin_limit, d_err);
+  return kvp::launch_status();
+}
+
 extern "C" const char* kv_status_string(int status) {
   switch (status) {
     case KV_OK: return "KV_OK";
@@ -32,4 +57,4 @@ extern "C" const char* kv_status_string(int status) {
   }
 }
 
-extern "C" int kv_abi_version(void) { return 4; }
+extern "C" int kv_abi_version(void) { return 5; }

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 4
+    assert lib.kv_abi_version() == 5
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -146,3 +146,9 @@ def test_bulk_gather_rejects_unsupported_shapes(lib):
                                     2049, N, N, 0, N, N) == -2
     assert lib.kv_cache_gather_bulk(0x1000, 0x2000, 0, 1, 8, 16, 8, 128, N, 0, N, N, 0, N, N, 0,
                                     N, N) == 0
+
+
+def test_diag_bounded_wait_rejects_bad_arguments(lib):
+    assert lib.kv_diag_bounded_wait(0, 0x1000, N) == -1
+    assert lib.kv_diag_bounded_wait((1 << 20) + 1, 0x1000, N) == -1
+    assert lib.kv_diag_bounded_wait(16, N, N) == -1

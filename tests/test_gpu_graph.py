@@ -115,3 +115,21 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk):
         e3 = oracle.cache_gather(kc_before, vc_before, 0, B, T, table, g0, g1, ko, vo)
         assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo)
         assert int(err.item()) == (e1 | e2 | e3) == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """The bounded wait used by the bulk-copy gather gives up on a barrier that
+    nothing completes, reports KV_ERR_TIMEOUT, and the next kernels run."""
+    lib = kv.load()
+    e = err_word()
+    rc = lib.kv_diag_bounded_wait(4096, e.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(e.item()) == kv.ERR_BITS["TIMEOUT"]
+    # the context is still usable: a normal call right after gives correct slots
+    q = torch.tensor([0, 3], dtype=torch.int32, device=dev())
+    p = torch.tensor([0, 1, 17], dtype=torch.int64, device=dev())
+    t = torch.tensor([[3, 4]], dtype=torch.int32, device=dev())
+    e2 = err_word()
+    s = kv.kv_slot_mapping_paged(q, p, t, 16, 8, max_num_tokens=5, err=e2)
+    assert s.cpu().tolist() == [48, 49, 65, -1, -1] and int(e2.item()) == 0
