@@ -766,41 +766,53 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
         src = torch.from_numpy(np.ascontiguousarray(src)) if isinstance(src, np.ndarray) else src
         h_stage[offs[n]:offs[n] + nbytes].copy_(src.contiguous().view(-1).view(torch.uint8))
         dev_in[n] = d_stage[offs[n]:offs[n] + nbytes].view(k[n].dtype).view(k[n].shape)
-    # the step's calls on the uploaded inputs
+    # the step's outputs (both slot mappings and the error word) packed in one
+    # device buffer, read back with one copy
     T, B, n_max, rows = w.block_size, w.num_blocks, w.max_num_tokens, k["rows"]
-    slot_p, slot_r, err = k["slot_p"], k["slot_r"], k["err"]
+    n_slot = k["slot_p"].numel()
+    d_out = torch.zeros(2 * n_slot * 8 + 256, dtype=torch.uint8, device=d_stage.device)
+    slot_p = d_out[:n_slot * 8].view(torch.int64)
+    slot_r = d_out[n_slot * 8:2 * n_slot * 8].view(torch.int64)
+    err = d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)
+    h_out = torch.empty_like(d_out, device="cpu").pin_memory()
     d = dev_in
-
-    def step():
+    # validated once; each step relaunches with the cached pointers
+    calls = [
         kv.kv_slot_mapping_paged(d["qsl"], d["pos"], d["table"], T, B, max_num_tokens=n_max,
-                                 slot_mapping=slot_p, err=err)
+                                 slot_mapping=slot_p, err=err, prepare=True),
         kv.kv_slot_mapping_range(d["qsl"], d["pos"], d["rs"], d["rl"], d["nr"], T, B,
-                                 max_num_tokens=n_max, slot_mapping=slot_r, err=err)
-        kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=err)
+                                 max_num_tokens=n_max, slot_mapping=slot_r, err=err,
+                                 prepare=True),
+        kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=err, prepare=True),
         kv.kv_cache_gather(k["kc"], k["vc"], d["table"], d["g0"], d["g1"], k_out=k["k_out"],
-                           v_out=k["v_out"], out_rows=rows, err=err)
-
-    h_out = {"slot_p": torch.empty_like(slot_p, device="cpu").pin_memory(),
-             "slot_r": torch.empty_like(slot_r, device="cpu").pin_memory(),
-             "err": torch.empty_like(err, device="cpu").pin_memory()}
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+                           v_out=k["v_out"], out_rows=rows, err=err, prepare=True),
+    ]
+    d2h = h_out.numel()
     times = []
     for s in range(steps):
         flush_l2(flush_buf)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         d_stage.copy_(h_stage, non_blocking=True)
-        step()
-        for n, h in h_out.items():
-            h.copy_(k[n], non_blocking=True)
+        for c in calls:
+            c()
+        h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
         times.append(time.perf_counter() - t0)
+    # what came back is the device path's answer on the same inputs
+    back_p = h_out[:n_slot * 8].view(torch.int64)
+    back_r = h_out[n_slot * 8:2 * n_slot * 8].view(torch.int64)
+    back_e = int(h_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)[0])
+    if (back_e != 0 or not torch.equal(back_p, k["slot_p"].cpu())
+            or not torch.equal(back_r, k["slot_r"].cpu())):
+        raise RuntimeError("end-to-end read-back differs from the device-resident step")
     med = statistics.median(times)
     return {"value": round(built.tokens / med, 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(med * 1e3, 3),
             "note": "median wall time of one step: one pinned H2D copy of the step's packed "
-                    "inputs, the four calls, D2H of both slot mappings and the error word, "
+                    "inputs, the four calls (prepared: validated once, relaunched with cached "
+                    "pointers), one D2H copy of both slot mappings and the error word, "
                     "stream synchronised"}
 
 

@@ -7,7 +7,7 @@ synthetic workloads live in ``workloads``.
 """
 from ._lib import (ERR_BITS, KV_EINVAL, KV_EUNSUPPORTED, KV_ECUDA, KV_OK, KVError,
                    MAX_GATHER_REQS, MAX_RANGES_PER_REQ, NULL_BLOCK_ID, PAD_SLOT_ID, load)
-from .ops import (kv_cache_gather, kv_cache_gather_range, kv_cache_write, kv_copy_blocks,
+from .ops import (Prepared, kv_cache_gather, kv_cache_gather_range, kv_cache_write, kv_copy_blocks,
                   kv_expand_kernel_blocks, kv_slot_mapping_paged, kv_slot_mapping_paged_cp,
                   kv_slot_mapping_range,
                   kv_table_from_ranges, new_error_word)
@@ -17,5 +17,5 @@ __all__ = [
     "MAX_GATHER_REQS", "MAX_RANGES_PER_REQ", "NULL_BLOCK_ID", "PAD_SLOT_ID", "load",
     "kv_cache_gather", "kv_cache_write", "kv_expand_kernel_blocks", "kv_slot_mapping_paged",
     "kv_slot_mapping_range", "new_error_word", "kv_table_from_ranges", "kv_cache_gather_range",
-    "kv_copy_blocks", "kv_slot_mapping_paged_cp",
+    "kv_copy_blocks", "kv_slot_mapping_paged_cp", "Prepared",
 ]

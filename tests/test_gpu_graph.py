@@ -5,7 +5,9 @@ valid while the batch changes ("Range-addressed KV cache blocks ...", The
 Innovation: stable slot-mapping values under CUDA graph capture;
 "Blocktabelle", CUDA-Graph-Padding).  Every launch here is sized by host
 arguments only, so a step captured once is replayed on new inputs written in
-place, and every replay must match the oracle bit for bit."""
+place, and every replay must match the oracle bit for bit.  The binding's
+prepared calls (validated once, relaunched with cached pointers) are the
+uncaptured form of the same replay and are held to the same bar."""
 import numpy as np
 import pytest
 import torch
@@ -50,8 +52,9 @@ def _batch(seed, R_pad, n_max, T, B, stride):
     return R, qsl, pos, table, g0, g1
 
 
+@pytest.mark.parametrize("mode", ["graph", "prepared"])
 @pytest.mark.parametrize("bulk", [False, True])
-def test_decode_step_captured_once_replayed_on_new_batches(bulk):
+def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode):
     T, B, H, D, stride, R_pad = 16, 512, 8, 128, 16, 32
     n_max = R_pad
     out_rows = R_pad * stride * T
@@ -78,14 +81,33 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk):
                            out_rows=out_rows, err=err, bulk=bulk)
 
     s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        step()  # warm-up outside capture
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
+    if mode == "graph":
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()  # warm-up outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        replay = graph.replay
+    else:
+        calls = [
+            kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
+                                     slot_mapping=slot, err=err, prepare=True),
+            kv.kv_cache_write(key, val, kc, vc, slot, err=err, prepare=True),
+            kv.kv_cache_gather(kc, vc, d_table, d_g0, d_g1, k_out=k_out, v_out=v_out,
+                               out_rows=out_rows, err=err, bulk=bulk, prepare=True),
+        ]
+        assert all(isinstance(c, kv.Prepared) for c in calls)
+        assert calls[0].result is slot and calls[2].result[0] is k_out and calls[2].result[1] is v_out
+
+        def replay():  # launches on the stream current at call time
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for c in calls:
+                    c()
+            torch.cuda.current_stream().wait_stream(s)
 
     for it, seed in enumerate([11, 12, 13]):
         R, qsl, pos, table, g0, g1 = _batch(seed, R_pad, n_max, T, B, stride)
@@ -100,7 +122,7 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk):
         key.copy_(new_k)
         val.copy_(new_v)
         err.zero_()
-        graph.replay()
+        replay()
         torch.cuda.synchronize()
         # oracle: the same step on the host
         exp_s, e1 = oracle.slot_mapping_paged(qsl, pos, table, R, n_max, T, B)
