@@ -208,8 +208,10 @@ class Built:
         self.name, self.desc, self.launches, self.tokens, self.keep = name, desc, launches, tokens, keep
 
 
-def build_decode(torch, kv, wl, dev, seed=1, extras=False):
-    w = wl.decode(seed)
+def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
+    # small: the same 256-token batch over a 20480-block pool and contexts
+    # U{512..1024} (a few GB on the device, for profiler captures)
+    w = wl.decode(seed, 20480, 1024) if small else wl.decode(seed)
     lay = w.layouts["G"]
     T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
@@ -854,8 +856,7 @@ def main():
     peak, peak_kind = load_peaks()
     flush_buf = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    built = BUILDERS[args.workload](torch, kv, wl, dev, **({} if args.workload == "decode"
-                                                          else {"small": args.small}))
+    built = BUILDERS[args.workload](torch, kv, wl, dev, small=args.small)
     for _ in range(args.warmup):
         flush_l2(flush_buf)
         for l in built.launches:

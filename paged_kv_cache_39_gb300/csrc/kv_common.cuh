@@ -107,11 +107,19 @@ struct RangeRowCheck {
 
   __device__ __forceinline__ void load(const int32_t* __restrict__ num_ranges,
                                        const int32_t* __restrict__ range_len, int row,
-                                       int32_t stride) {
+                                       int32_t stride, bool vec4 = false) {
     r = row;
     const int32_t* rl = range_len + (int64_t)row * stride;
+    if (vec4) {  // the caller checked: stride >= 4, rows 16-byte aligned
+      const int4 v = *reinterpret_cast<const int4*>(rl);
+      l4[0] = v.x;
+      l4[1] = v.y;
+      l4[2] = v.z;
+      l4[3] = v.w;
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) l4[i] = i < stride ? rl[i] : 1;
+      for (int i = 0; i < 4; ++i) l4[i] = i < stride ? rl[i] : 1;
+    }
     n = num_ranges[row];
   }
   __device__ __forceinline__ bool malformed(const int32_t* __restrict__ range_len,

@@ -292,14 +292,14 @@ def tiny(seed: int = 0) -> Workload:
                     notes="prompts from position 0; max_num_tokens rounded up to 256")
 
 
-def decode(seed: int = 1) -> Workload:
-    """256 decode requests, context U{512..4096}, one new token each, 40960-block pool."""
+def decode(seed: int = 1, num_blocks: int = 40960, ctx_max: int = 4096) -> Workload:
+    """256 decode requests, context U{512..ctx_max}, one new token each, num_blocks pool."""
     rng = np.random.default_rng(seed)
-    T, B, R = 16, 40960, 256
-    ctx = rng.integers(512, 4097, size=R)
+    T, B, R = 16, num_blocks, 256
+    ctx = rng.integers(512, ctx_max + 1, size=R)
     nblocks = np.array([blocks_for(int(c), T) for c in ctx], dtype=np.int64)
     assert int(nblocks.sum()) < B - 1
-    stride = table_stride_for(blocks_for(4096, T), T)
+    stride = table_stride_for(blocks_for(ctx_max, T), T)
     lay_g = _runs_layout(rng, nblocks, 4, B, R, stride, RANGE_CAP, packed=False)
     positions = (ctx - 1).astype(np.int64)
     g0 = np.zeros(R, dtype=np.int32)

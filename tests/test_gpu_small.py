@@ -154,20 +154,30 @@ def random_slot_case(rng):
     return T, R, q.astype(np.int32), N, n_max, stride, B, table, pos
 
 
+# Batches that fit one wave of CTAs run one token per thread; padding
+# max_num_tokens past that (200k) makes the same tokens run 4 per thread, with
+# the lane windows and warp descriptor cache carried across a thread's tokens.
+PADS = [0, 200_000]
+
+
+@pytest.mark.parametrize("pad", PADS)
 @pytest.mark.parametrize("seed", range(40))
-def test_paged_adversarial(seed):
+def test_paged_adversarial(seed, pad):
     rng = np.random.default_rng(1000 + seed)
     T, R, q, N, n_max, stride, B, table, pos = random_slot_case(rng)
+    n_max += pad
     exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
     s, e = run_paged(q, pos, table, N, n_max, T, B)
     assert e == exp_e
     assert np.array_equal(s, exp_s)
 
 
+@pytest.mark.parametrize("pad", PADS)
 @pytest.mark.parametrize("seed", range(40))
-def test_range_adversarial(seed):
+def test_range_adversarial(seed, pad):
     rng = np.random.default_rng(2000 + seed)
     T, R, q, N, n_max, stride, B, table, pos = random_slot_case(rng)
+    n_max += pad
     rstride = int(rng.choice([1, 4, 40, 256]))
     rows = max(R, 1)
     rs = rng.integers(-2, B + 2, size=(rows, rstride)).astype(np.int32)
@@ -183,8 +193,9 @@ def test_range_adversarial(seed):
     assert np.array_equal(s, exp_s)
 
 
+@pytest.mark.parametrize("pad", PADS)
 @pytest.mark.parametrize("seed", range(6))
-def test_range_equals_paged_with_256_ranges(seed):
+def test_range_equals_paged_with_256_ranges(seed, pad):
     """Full descriptor rows (256 ranges, 8 warp chunks) agree with the table."""
     rng = np.random.default_rng(3000 + seed)
     T, R = 16, 3
@@ -206,9 +217,10 @@ def test_range_equals_paged_with_256_ranges(seed):
     pos = np.concatenate([rng.integers(0, int(lens[r].sum()) * T + 40, size=tok[r])
                           for r in range(R)]).astype(np.int64)
     N = int(q[-1])
-    sp, ep = run_paged(q, pos, table, N, N, T, B)
-    sr, er = run_range(q, pos, rs, rl, nr, N, N, T, B)
-    exp, ee = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+    n_max = N + pad
+    sp, ep = run_paged(q, pos, table, N, n_max, T, B)
+    sr, er = run_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    exp, ee = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
     assert ep == er == ee == 0
     assert np.array_equal(sr, exp) and np.array_equal(sp, exp)
 
@@ -352,9 +364,10 @@ def test_expand_random_parity(k, extra):
     assert np.array_equal(out.cpu().numpy(), exp)
 
 
-@pytest.mark.parametrize("n_max", [1000, 700_000, 1_300_000, 2_600_000])
+@pytest.mark.parametrize("n_max", [1000, 150_000, 400_000, 700_000, 1_300_000, 2_600_000])
 def test_slot_mapping_tile_variants(n_max):
-    """Large batches switch to 8 and 16 tokens per thread; results are unchanged."""
+    """Batches past one wave of CTAs switch to 4, 8 and 16 tokens per thread;
+    results are unchanged."""
     rng = np.random.default_rng(n_max)
     T, R = 16, 37
     lens = rng.multinomial(n_max - 5, np.ones(R) / R)
