@@ -138,16 +138,18 @@ class ClockSampler:
 
 
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of the sources a kernel is built from (its .cu file and the common header)."""
+    """Hash of the sources a kernel is built from (its .cu file and the headers)."""
     files = {"cache_gather_kernel": "kv_cache_gather.cu", "cache_write_kernel": "kv_cache_write.cu",
              "slot_mapping_paged_kernel": "kv_slot_mapping.cu",
              "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu",
              "cache_gather_range_kernel": "kv_cache_gather.cu",
              "table_from_ranges_kernel": "kv_range_table.cu",
              "copy_blocks_kernel": "kv_copy_blocks.cu",
-             "cache_gather_bulk_kernel": "kv_cache_gather.cu"}
+             "cache_gather_bulk_kernel": "kv_cache_gather.cu",
+             "slot_write_kernel": "kv_slot_write.cu"}
     h = hashlib.sha256()
-    for f in (files[kernel], "kv_common.cuh"):
+    csrc = os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc")
+    for f in [files[kernel]] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
         with open(os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -197,6 +199,11 @@ def range_bytes(N, n_max, R, nr):
 
 def write_bytes(L, N_valid, N, row_bytes):
     return L * N_valid * row_bytes * 4 + N * 8
+
+
+def fused_bytes(slot_bytes, L, N_valid, N, row_bytes):
+    """Slot map plus write, without the write's re-read of the slot mapping."""
+    return slot_bytes + write_bytes(L, N_valid, N, row_bytes) - N * 8
 
 
 def gather_bytes(rows, row_bytes, blocks, R):
@@ -250,7 +257,18 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
     if extras:
         table2 = torch.empty_like(table)
         slot_cp = torch.empty_like(slot_p)
+        slot_f = torch.empty_like(slot_p)
         launches += [
+            Launch("slot_mapping_paged_write", "slot_write_kernel",
+                   lambda: kv.kv_slot_mapping_paged_write(qsl, pos, table, T, B, key, val, kc, vc,
+                                                          max_num_tokens=n_max,
+                                                          slot_mapping=slot_f, err=err),
+                   fused_bytes(slotmap_bytes(N, n_max, R), 1, N, N, rb), N),
+            Launch("slot_mapping_range_write", "slot_write_kernel",
+                   lambda: kv.kv_slot_mapping_range_write(qsl, pos, rs, rl, nr, T, B, key, val,
+                                                          kc, vc, max_num_tokens=n_max,
+                                                          slot_mapping=slot_f, err=err),
+                   fused_bytes(range_bytes(N, n_max, R, lay.num_ranges), 1, N, N, rb), N),
             Launch("slot_mapping_paged_cp[W=4,rank1]", "slot_mapping_paged_kernel",
                    lambda: kv.kv_slot_mapping_paged_cp(qsl, pos, table, T, B, 4, 1, 1,
                                                        max_num_tokens=n_max, slot_mapping=slot_cp,
@@ -294,6 +312,7 @@ def build_mixed(torch, kv, wl, dev, small=False):
     vc = torch.full((L, B, T, H, D), 0x3C01, dtype=torch.int16, device=dev).view(torch.bfloat16)
     slot_p = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
     slot_r = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
+    slot_f = torch.empty(w.max_num_tokens, dtype=torch.int64, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     N, n_max, R = w.num_tokens, w.max_num_tokens, w.num_reqs
     # copy-on-write fork of 1024 blocks (every layer): disjoint sources and targets
@@ -312,6 +331,17 @@ def build_mixed(torch, kv, wl, dev, small=False):
         Launch("cache_write", "cache_write_kernel",
                lambda: kv.kv_cache_write(key, val, kc, vc, slot_p, err=err),
                write_bytes(L, N, N, w.row_bytes), N * L),
+        Launch("slot_mapping_paged_write", "slot_write_kernel",
+               lambda: kv.kv_slot_mapping_paged_write(qsl, pos, table, T, B, key, val, kc, vc,
+                                                      max_num_tokens=n_max, slot_mapping=slot_f,
+                                                      err=err),
+               fused_bytes(slotmap_bytes(N, n_max, R), L, N, N, w.row_bytes), N * L),
+        Launch("slot_mapping_range_write", "slot_write_kernel",
+               lambda: kv.kv_slot_mapping_range_write(qsl, pos, rs, rl, nr, T, B, key, val, kc,
+                                                      vc, max_num_tokens=n_max,
+                                                      slot_mapping=slot_f, err=err),
+               fused_bytes(range_bytes(N, n_max, R, lay.num_ranges), L, N, N, w.row_bytes),
+               N * L),
         Launch("copy_blocks[cow 1024]", "copy_blocks_kernel",
                lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err),
                n_cow * L * T * w.row_bytes * 4 + n_cow * 8, n_cow * L),
@@ -708,20 +738,20 @@ def run_reference(args, rk):
     print(json.dumps(line), flush=True)
 
 
-def graph_decode(torch, built, steps, flush_buf):
-    """The same step captured once in a CUDA graph and replayed (how a serving
-    loop runs decode steps); L2 flushed between replays, outside the events."""
+def graph_replay_ms(torch, fns, steps, flush_buf):
+    """Mean device time (ms) of one replay of `fns` captured once in a CUDA
+    graph; L2 flushed between replays, outside the events."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for l in built.launches:
-            l.fn()
+        for fn in fns:
+            fn()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for l in built.launches:
-            l.fn()
+        for fn in fns:
+            fn()
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
@@ -735,9 +765,75 @@ def graph_decode(torch, built, steps, flush_buf):
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in evs) / steps
     del g
+    return ms
+
+
+def graph_decode(torch, built, steps, flush_buf):
+    """The same step captured once in a CUDA graph and replayed (how a serving
+    loop runs decode steps)."""
+    ms = graph_replay_ms(torch, [l.fn for l in built.launches], steps, flush_buf)
     return {"ms_per_step": round(ms, 4), "value": round(built.tokens / (ms * 1e-3), 1),
             "unit": "tokens/s", "steps": steps,
-            "note": "the four calls captured once in a CUDA graph, one replay per step"}
+            "note": "the four calls captured once in a CUDA graph, one replay per step; "
+                    "L2 flushed between replays"}
+
+
+def write_slotmap_decode(torch, kv, built, kernels, reps, steps, flush_buf, stream, peak):
+    """Slot map + KV write of the decode batch: the separate calls (from the
+    step's per-launch times) against the fused calls (timed here, L2 flushed
+    before every launch), and each pair captured in a CUDA graph."""
+    k = built.keep
+    w, lay = k["w"], k["lay"]
+    T, B, n_max = w.block_size, w.num_blocks, w.max_num_tokens
+    q, p, kc, vc, key, val, err = k["qsl"], k["pos"], k["kc"], k["vc"], k["key"], k["val"], k["err"]
+    slot_p, slot_r = k["slot_p"], k["slot_r"]
+    slot_f = torch.empty_like(slot_p)
+    fused = {
+        "paged": lambda: kv.kv_slot_mapping_paged_write(q, p, k["table"], T, B, key, val, kc, vc,
+                                                        max_num_tokens=n_max, slot_mapping=slot_f,
+                                                        err=err),
+        "range": lambda: kv.kv_slot_mapping_range_write(q, p, k["rs"], k["rl"], k["nr"], T, B,
+                                                        key, val, kc, vc, max_num_tokens=n_max,
+                                                        slot_mapping=slot_f, err=err),
+    }
+    sep = {l.name: l.fn for l in built.launches}
+    fb = Built("fused", "", [Launch("slot_mapping_paged_write", "slot_write_kernel",
+                                    fused["paged"], 0, w.num_tokens),
+                             Launch("slot_mapping_range_write", "slot_write_kernel",
+                                    fused["range"], 0, w.num_tokens)], w.num_tokens, k)
+    for _ in range(3):
+        for l in fb.launches:
+            l.fn()
+    per = time_each(torch, fb, reps, flush_buf, stream)
+    us_f = {n: sum(t) / len(t) * 1e3 for n, t in zip(("paged", "range"), per)}
+    tw = kernels["cache_write"]["us"]
+    us_sep = {"paged": kernels["slot_mapping_paged"]["us"] + tw,
+              "range": kernels["slot_mapping_range"]["us"] + tw}
+    graphs = {
+        "paged": [sep["slot_mapping_paged"], sep["cache_write"]],
+        "range": [sep["slot_mapping_range"],
+                  lambda: kv.kv_cache_write(key, val, kc, vc, slot_r, err=err)],
+        "paged_fused": [fused["paged"]],
+        "range_fused": [fused["range"]],
+    }
+    g_us = {n: graph_replay_ms(torch, fns, steps, flush_buf) * 1e3 for n, fns in graphs.items()}
+    n = built.tokens
+    if not torch.equal(slot_f, slot_r) or not torch.equal(slot_p, slot_r):
+        raise RuntimeError("fused and separate slot mappings differ")
+    return {
+        "paged": round(n / (us_sep["paged"] * 1e-6), 1),
+        "range": round(n / (us_sep["range"] * 1e-6), 1),
+        "paged_fused": round(n / (us_f["paged"] * 1e-6), 1),
+        "range_fused": round(n / (us_f["range"] * 1e-6), 1),
+        "us": {"paged": round(us_sep["paged"], 2), "range": round(us_sep["range"], 2),
+               "paged_fused": round(us_f["paged"], 2), "range_fused": round(us_f["range"], 2)},
+        "graph_replay_us": {n_: round(v, 2) for n_, v in g_us.items()},
+        "graph_replay_tokens_per_s": {n_: round(n / (v * 1e-6), 1) for n_, v in g_us.items()},
+        "note": "paged/range: the slot-map launch plus the write launch, each timed with L2 "
+                "flushed before it; *_fused: kv_slot_mapping_{paged,range}_write, one launch, "
+                "timed the same way; graph_replay: each pair captured in one CUDA graph, L2 "
+                "flushed between replays",
+    }
 
 
 # --------------------------------------------------------------------------
@@ -907,12 +1003,9 @@ def main():
             "gpu_launches": args.steps * sum(l.launches for l in built.launches),
             "clocks": clocks.summary()}
     if built.name == "decode":
-        t_paged = kernels["slot_mapping_paged"]["us"]
-        t_range = kernels["slot_mapping_range"]["us"]
-        t_write = kernels["cache_write"]["us"]
-        line["write_slotmap_tokens_per_s"] = {
-            "paged": round(built.tokens / ((t_paged + t_write) * 1e-6), 1),
-            "range": round(built.tokens / ((t_range + t_write) * 1e-6), 1)}
+        line["write_slotmap_tokens_per_s"] = write_slotmap_decode(
+            torch, kv, built, kernels, args.detail_reps * 10, min(args.steps, 500), flush_buf,
+            stream, peak)
         line["gather_GBps"] = kernels["cache_gather"]["GB/s"]
         line["graph"] = graph_decode(torch, built, min(args.steps, 500), flush_buf)
         line["e2e"] = e2e_decode(torch, kv, built, min(args.steps, 200), flush_buf, stream)
@@ -972,7 +1065,11 @@ def detail(torch, kv, wl, dev, args, flush_buf, stream, peak):
             tw = rep["cache_write"]["us"]
             entry["write_slotmap_tokens_per_s"] = {
                 "paged": round(b.tokens / ((rep["slot_mapping_paged"]["us"] + tw) * 1e-6), 1),
-                "range": round(b.tokens / ((rep["slot_mapping_range"]["us"] + tw) * 1e-6), 1)}
+                "range": round(b.tokens / ((rep["slot_mapping_range"]["us"] + tw) * 1e-6), 1),
+                "paged_fused": round(b.tokens / (rep["slot_mapping_paged_write"]["us"] * 1e-6),
+                                     1),
+                "range_fused": round(b.tokens / (rep["slot_mapping_range_write"]["us"] * 1e-6),
+                                     1)}
         out[name] = entry
         del b
         torch.cuda.synchronize()

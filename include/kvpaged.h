@@ -1,11 +1,13 @@
 /*
  * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
  *
- * Ten calls, each one kernel launch on the caller's stream:
+ * Twelve calls, each one kernel launch on the caller's stream:
  *   kv_slot_mapping_paged    token -> cache slot through a block table
  *   kv_slot_mapping_paged_cp the same, for one rank of context parallelism
  *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
  *   kv_cache_write           scatter new K/V rows into the paged caches
+ *   kv_slot_mapping_paged_write  slot mapping and KV write in one launch
+ *   kv_slot_mapping_range_write  the same through contiguous ranges
  *   kv_cache_gather          gather a request's K/V through its block table
  *   kv_cache_gather_bulk     the same gather, moved by bulk (TMA) copies
  *   kv_expand_kernel_blocks  manager-size block table -> kernel-size blocks
@@ -202,7 +204,8 @@ int kv_slot_mapping_range(const int32_t* query_start_loc, const int64_t* positio
  *   s >= num_blocks*block_size  -> skipped, KV_ERR_BAD_SLOT
  *   otherwise cache row (l * num_blocks + s / block_size) * block_size + s % block_size
  *   of k_cache (v_cache) receives key[l][t] (value[l][t]) bit for bit.
- * Two tokens with the same slot race (one of the rows wins).
+ * Two tokens with the same slot race: each 16-byte piece of the row comes
+ * from one of them, not necessarily the same one for every piece.
  * Errors: KV_EINVAL for a null or non-16-byte-aligned K/V pointer, negative
  * sizes, num_blocks < 1, block_size <= 0, num_kv_heads <= 0 or head_dim <= 0;
  * KV_EUNSUPPORTED when num_kv_heads * head_dim * 2 is not a multiple of 16.
@@ -211,6 +214,55 @@ int kv_cache_write(const void* key, const void* value, void* k_cache, void* v_ca
                    const int64_t* slot_mapping, int32_t num_tokens, int32_t num_layers,
                    int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                    int32_t head_dim, int32_t* d_err, kv_stream_t stream);
+
+/*
+ * kv_slot_mapping_paged_write -- kv_slot_mapping_paged, then kv_cache_write on
+ * the slots it produced, in one launch.
+ *
+ * The slot of [BT] Datenfluss and the write by slot of [BT] Verantwortung
+ * and [VBM] Deep Dive 8 with no trip through memory in between: each token's
+ * K and V rows go straight to the slot computed for it.
+ *
+ *   query_start_loc .. num_blocks, slot_mapping  as kv_slot_mapping_paged;
+ *                     slot_mapping is still written in full (PAD tail
+ *                     included), for the attention kernels that read it.
+ *   key, value        bf16 [num_layers, num_tokens, num_kv_heads, head_dim].
+ *   k_cache, v_cache  bf16 [num_layers, num_blocks, block_size, num_kv_heads, head_dim].
+ *
+ * Results (slot_mapping, cache bytes, error bits) are exactly those of the
+ * two calls in sequence; since a slot produced here is never in block 0 nor
+ * past the pool, the write half adds no error bit of its own.  Tokens given
+ * the same slot (a table that repeats a block) race as in kv_cache_write.
+ * Errors: the union of the two calls' argument checks.
+ */
+int kv_slot_mapping_paged_write(const int32_t* query_start_loc, const int64_t* positions,
+                                const int32_t* block_table, int32_t table_stride,
+                                int32_t num_reqs, int32_t num_tokens, int32_t max_num_tokens,
+                                int32_t block_size, int64_t num_blocks, const void* key,
+                                const void* value, void* k_cache, void* v_cache,
+                                int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                                int64_t* slot_mapping, int32_t* d_err, kv_stream_t stream);
+
+/*
+ * kv_slot_mapping_range_write -- kv_slot_mapping_range, then kv_cache_write on
+ * the slots it produced, in one launch ([RNG] The Innovation for the block,
+ * otherwise as kv_slot_mapping_paged_write).
+ *
+ *   range_start, range_len, num_ranges, range_stride  as kv_slot_mapping_range.
+ *   other arguments   as kv_slot_mapping_paged_write.
+ *
+ * Results are exactly those of kv_slot_mapping_range followed by
+ * kv_cache_write, including KV_ERR_BAD_RANGE for every malformed row
+ * r < num_reqs.  Errors: as kv_slot_mapping_range and kv_cache_write.
+ */
+int kv_slot_mapping_range_write(const int32_t* query_start_loc, const int64_t* positions,
+                                const int32_t* range_start, const int32_t* range_len,
+                                const int32_t* num_ranges, int32_t range_stride,
+                                int32_t num_reqs, int32_t num_tokens, int32_t max_num_tokens,
+                                int32_t block_size, int64_t num_blocks, const void* key,
+                                const void* value, void* k_cache, void* v_cache,
+                                int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                                int64_t* slot_mapping, int32_t* d_err, kv_stream_t stream);
 
 /*
  * kv_cache_gather -- read each request's K/V through its block table into

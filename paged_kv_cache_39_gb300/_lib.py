@@ -42,6 +42,10 @@ SIGNATURES = {
                               ctypes.c_int),
     "kv_cache_write": ([_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _P],
                        ctypes.c_int),
+    "kv_slot_mapping_paged_write": ([_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P, _P, _P,
+                                     _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "kv_slot_mapping_range_write": ([_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I64, _P,
+                                     _P, _P, _P, _I32, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "kv_cache_gather": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P, _P,
                          _I64, _P, _P], ctypes.c_int),
     "kv_cache_gather_bulk": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P,

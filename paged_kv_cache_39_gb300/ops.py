@@ -29,6 +29,8 @@ __all__ = [
     "kv_slot_mapping_paged_cp",
     "kv_slot_mapping_range",
     "kv_cache_write",
+    "kv_slot_mapping_paged_write",
+    "kv_slot_mapping_range_write",
     "kv_cache_gather",
     "kv_expand_kernel_blocks",
     "kv_table_from_ranges",
@@ -227,6 +229,71 @@ def kv_cache_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor
             T, H, D, _err_ptr(err, dev))
     return _run("kv_cache_write", args, dev, (key, value, k_cache, v_cache, slot_mapping, err),
                 None, prepare)
+
+
+def _rows_check(key, value, k_cache, v_cache, dev, n):
+    """Shapes of the write half of the fused calls: (L, H, D, row arguments)."""
+    _need(key, "key", torch.bfloat16, dev)
+    _need(value, "value", torch.bfloat16, dev)
+    L, B, T, H, D = _cache_dims(k_cache, v_cache, dev)
+    if key.dim() != 4 or key.shape[0] != L or key.shape[2:] != (H, D) or value.shape != key.shape:
+        raise ValueError("key/value must be [num_layers, num_tokens, kv_heads, head_dim]")
+    if n > key.shape[1]:
+        raise ValueError("num_tokens exceeds key rows")
+    if n != key.shape[1] and L > 1:
+        raise ValueError("num_tokens must equal key.shape[1] for multi-layer writes")
+    return (_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), L, H, D)
+
+
+def kv_slot_mapping_paged_write(query_start_loc: torch.Tensor, positions: torch.Tensor,
+                                block_table: torch.Tensor, block_size: int, num_blocks: int,
+                                key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, max_num_tokens: Optional[int] = None,
+                                slot_mapping: Optional[torch.Tensor] = None,
+                                num_tokens: Optional[int] = None,
+                                err: Optional[torch.Tensor] = None, prepare: bool = False):
+    """kv_slot_mapping_paged then kv_cache_write on its slots, in one launch.
+
+    ``num_blocks`` must equal the caches' block count.  Returns slot_mapping."""
+    dev, R, n, n_max, slot_mapping = _slot_common(query_start_loc, positions, max_num_tokens,
+                                                  slot_mapping, num_tokens)
+    _table_check(block_table, dev, R)
+    rows = _rows_check(key, value, k_cache, v_cache, dev, n)
+    if int(num_blocks) != k_cache.shape[1]:
+        raise ValueError("num_blocks differs from the caches' block count")
+    if int(block_size) != k_cache.shape[2]:
+        raise ValueError("block_size differs from the caches' block size")
+    args = (_ptr(query_start_loc), _ptr(positions), _ptr(block_table), block_table.shape[1], R,
+            n, n_max, int(block_size), int(num_blocks), *rows, _ptr(slot_mapping),
+            _err_ptr(err, dev))
+    return _run("kv_slot_mapping_paged_write", args, dev,
+                (query_start_loc, positions, block_table, key, value, k_cache, v_cache,
+                 slot_mapping, err), slot_mapping, prepare)
+
+
+def kv_slot_mapping_range_write(query_start_loc: torch.Tensor, positions: torch.Tensor,
+                                range_start: torch.Tensor, range_len: torch.Tensor,
+                                num_ranges: torch.Tensor, block_size: int, num_blocks: int,
+                                key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                                v_cache: torch.Tensor, max_num_tokens: Optional[int] = None,
+                                slot_mapping: Optional[torch.Tensor] = None,
+                                num_tokens: Optional[int] = None,
+                                err: Optional[torch.Tensor] = None, prepare: bool = False):
+    """kv_slot_mapping_range then kv_cache_write on its slots, in one launch."""
+    dev, R, n, n_max, slot_mapping = _slot_common(query_start_loc, positions, max_num_tokens,
+                                                  slot_mapping, num_tokens)
+    _ranges_check(range_start, range_len, num_ranges, dev, R)
+    rows = _rows_check(key, value, k_cache, v_cache, dev, n)
+    if int(num_blocks) != k_cache.shape[1]:
+        raise ValueError("num_blocks differs from the caches' block count")
+    if int(block_size) != k_cache.shape[2]:
+        raise ValueError("block_size differs from the caches' block size")
+    args = (_ptr(query_start_loc), _ptr(positions), _ptr(range_start), _ptr(range_len),
+            _ptr(num_ranges), range_start.shape[1], R, n, n_max, int(block_size),
+            int(num_blocks), *rows, _ptr(slot_mapping), _err_ptr(err, dev))
+    return _run("kv_slot_mapping_range_write", args, dev,
+                (query_start_loc, positions, range_start, range_len, num_ranges, key, value,
+                 k_cache, v_cache, slot_mapping, err), slot_mapping, prepare)
 
 
 def _gather_outputs(k_cache, gather_start, gather_end, k_out, v_out, out_rows, H, D, dev):

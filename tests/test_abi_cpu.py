@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 5
+    assert lib.kv_abi_version() == 6
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -152,3 +152,27 @@ def test_diag_bounded_wait_rejects_bad_arguments(lib):
     assert lib.kv_diag_bounded_wait(0, 0x1000, N) == -1
     assert lib.kv_diag_bounded_wait((1 << 20) + 1, 0x1000, N) == -1
     assert lib.kv_diag_bounded_wait(16, N, N) == -1
+
+
+def test_fused_slot_write_rejects_bad_arguments(lib):
+    # kv_slot_mapping_paged_write(qsl, pos, table, stride, R, N, N_max, T, B,
+    #                             key, value, k_cache, v_cache, L, H, D, slots, err, stream)
+    P = lib.kv_slot_mapping_paged_write
+    assert P(N, N, N, 0, -1, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == -1
+    assert P(N, N, N, 0, 0, 0, 0, 16, 8, N, N, N, N, -1, 8, 128, N, N, N) == -1
+    assert P(N, N, N, 0, 0, 0, 0, 16, 8, N, N, N, N, 1, 3, 5, N, N, N) == -2  # 30-byte rows
+    assert P(N, N, N, -1, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == -1
+    # one token to write but no key / a misaligned key
+    assert P(N, 0x1000, N, 0, 0, 1, 1, 16, 8, N, 0x2000, 0x3000, 0x4000, 1, 8, 128, 0x5000, N,
+             N) == -1
+    assert P(N, 0x1000, N, 0, 0, 1, 1, 16, 8, 0x1008, 0x2000, 0x3000, 0x4000, 1, 8, 128, 0x5000,
+             N, N) == -1
+    assert P(N, N, N, 0, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, 0x1002, N) == -1  # err
+    assert P(N, N, N, 0, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == 0  # empty
+    # kv_slot_mapping_range_write(qsl, pos, rs, rl, nr, rstride, R, N, N_max, T, B,
+    #                             key, value, k_cache, v_cache, L, H, D, slots, err, stream)
+    Q = lib.kv_slot_mapping_range_write
+    assert Q(N, N, N, N, N, 257, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == -2
+    assert Q(N, N, N, N, N, -1, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == -1
+    assert Q(0x1000, N, N, N, N, 4, 1, 0, 0, 16, 8, N, N, N, N, 1, 8, 128, N, N, N) == -1
+    assert Q(N, N, N, N, N, 4, 0, 0, 0, 16, 8, N, N, N, N, 1, 8, 64, N, N, N) == 0

@@ -15,14 +15,10 @@ import torch
 import oracle
 import paged_kv_cache_39_gb300 as kv
 from paged_kv_cache_39_gb300 import workloads as wl
-from gpu_helpers import (bits, cuda, dev, device_rows_equal, err_word, free_bytes, rows_view,
-                         sample_host_check)
+from gpu_helpers import (FILL, SAMPLE, bits, check_write, cuda, dev, device_rows_equal, err_word,
+                         filled_cache, free_bytes, rows_view, sample_host_check)
 
 pytestmark = pytest.mark.gpu
-
-FILL = 0x3C01  # bf16 bit pattern of the caches before the write (1.0078125)
-SAMPLE = 2048
-
 
 @pytest.fixture(autouse=True)
 def _device():
@@ -32,10 +28,6 @@ def _device():
     yield
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-
-
-def filled_cache(shape):
-    return torch.full(shape, FILL, dtype=torch.int16, device=dev()).view(torch.bfloat16)
 
 
 def slot_maps_match(w, lay, check_range=True):
@@ -60,38 +52,6 @@ def slot_maps_match(w, lay, check_range=True):
         assert np.array_equal(sr.cpu().numpy(), exp_r)
         assert np.array_equal(exp_r, exp)  # range == paged slot for slot
     return sp, exp
-
-
-def check_write(key, val, kc, vc, slots_host, L, N, B, T, E, rng):
-    """Oracle destination rows; full device check; sampled host check; untouched rows."""
-    dest, exp_e = oracle.write_rows(slots_host, N, L, B, T)
-    flat_dest = dest.reshape(-1)
-    valid = np.nonzero(flat_dest >= 0)[0]
-    # every written row holds its token's K/V row
-    src_k = rows_view(key, E)
-    src_v = rows_view(val, E)
-    kr, vr = rows_view(kc, E), rows_view(vc, E)
-    for s in range(0, len(valid), 1 << 16):
-        sel = torch.from_numpy(valid[s:s + (1 << 16)]).to(dev())
-        drow = torch.from_numpy(flat_dest[valid[s:s + (1 << 16)]]).to(dev())
-        assert torch.equal(kr.index_select(0, drow), src_k.index_select(0, sel))
-        assert torch.equal(vr.index_select(0, drow), src_v.index_select(0, sel))
-    # sampled host check through the oracle's per-row arithmetic
-    pick = rng.choice(len(valid), size=min(SAMPLE, len(valid)), replace=False)
-    for i in valid[pick][:256]:
-        l, t = divmod(int(i), N)
-        got = kr[int(flat_dest[i])].cpu().numpy().view(np.uint16)
-        assert np.array_equal(got, src_k[l * N + t].cpu().numpy().view(np.uint16))
-    # nothing else changed: rows differing from the fill pattern are exactly the written ones
-    fill64 = torch.tensor([FILL], dtype=torch.int16).repeat(4).view(torch.int64).item()
-    changed = 0
-    for c in (kc, vc):
-        per_layer = c.view(L, -1)
-        for l in range(L):
-            v64 = per_layer[l].view(torch.int16).view(-1, E).view(torch.int64)
-            changed += int((v64 != fill64).any(dim=1).sum().item())
-    assert changed == 2 * len(np.unique(flat_dest[valid]))
-    return exp_e
 
 
 def test_decode_full():

@@ -1,0 +1,138 @@
+"""GPU parity of the fused slot-mapping + KV write calls.
+
+kv_slot_mapping_paged_write (kv_slot_mapping_range_write) must give exactly
+what the oracle's paged (range) slot map followed by the oracle's KV write
+gives: the same slot mapping with its PAD tail, the same cache bytes and the
+same error word ("Blocktabelle", Datenfluss and Verantwortung;
+"Range-addressed KV cache blocks ...", The Innovation).  Two tokens given the
+same slot (a table that repeats a block) race for it in either form, one
+16-byte store at a time; there each 16-byte piece of the row must be one of
+theirs, and every other row is compared exactly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_39_gb300 as kv
+from paged_kv_cache_39_gb300 import workloads as wl
+from gpu_helpers import (bits, check_write, cuda, dev, err_word, filled_cache, free_bytes,
+                         random_slot_case)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kv.load()
+    torch.cuda.set_device(dev())
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def random_ranges(rng, rows, B):
+    rstride = int(rng.choice([1, 4, 40, 256]))
+    rs = rng.integers(-2, B + 2, size=(rows, rstride)).astype(np.int32)
+    rl = rng.integers(-1, 12, size=(rows, rstride)).astype(np.int32)
+    if rng.random() < 0.5:
+        rl = np.maximum(rl, 1)
+    nr = rng.integers(0, rstride + 1, size=rows).astype(np.int32)
+    if rng.random() < 0.3:
+        nr[rng.integers(0, rows)] = rstride + 1
+    return rs, rl, nr
+
+
+ROW_SHAPES = [(1, 8), (8, 64), (8, 128), (16, 128), (2, 72)]  # 16 B .. 4 KiB rows
+
+
+@pytest.mark.parametrize("kind", ["paged", "range"])
+@pytest.mark.parametrize("seed", range(30))
+def test_fused_adversarial(seed, kind):
+    rng = np.random.default_rng(7000 + seed)
+    T, R, q, N, n_max, stride, B, table, pos = random_slot_case(rng)
+    H, D = ROW_SHAPES[seed % len(ROW_SHAPES)]
+    L = 1 + seed % 3
+    if kind == "paged":
+        exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
+    else:
+        rs, rl, nr = random_ranges(rng, max(R, 1), B)
+        exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    key = wl.bf16_normal((L, N, H, D), 40 + seed)
+    val = wl.bf16_normal((L, N, H, D), 80 + seed)
+    kc = wl.bf16_normal((L, B, T, H, D), 120 + seed)
+    vc = wl.bf16_normal((L, B, T, H, D), 160 + seed)
+    kb, vb = bits(key), bits(val)
+    # slots that several tokens share race; the oracle writes the others
+    s_tok = exp_s[:N]
+    valid = s_tok[s_tok >= 0]
+    uniq, counts = np.unique(valid, return_counts=True)
+    shared = uniq[counts > 1]
+    s_unique = np.where(np.isin(s_tok, shared), -1, s_tok)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_we = oracle.cache_write(kb, vb, ek, ev, s_unique, B, T)
+    assert exp_we == 0  # the slot map never yields a slot the write refuses
+
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    slot = torch.full((n_max,), 12345, dtype=torch.int64, device=dev())
+    e = err_word()
+    if kind == "paged":
+        kv.kv_slot_mapping_paged_write(cuda(q), cuda(pos), cuda(table), T, B, key.to(dev()),
+                                       val.to(dev()), kc_d, vc_d, max_num_tokens=n_max,
+                                       slot_mapping=slot, num_tokens=N, err=e)
+    else:
+        kv.kv_slot_mapping_range_write(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B,
+                                       key.to(dev()), val.to(dev()), kc_d, vc_d,
+                                       max_num_tokens=n_max, slot_mapping=slot, num_tokens=N,
+                                       err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(slot.cpu().numpy(), exp_s)
+    gk, gv = bits(kc_d), bits(vc_d)
+    for s in shared:
+        b, o = divmod(int(s), T)
+        toks = np.nonzero(s_tok == s)[0]
+        for l in range(L):
+            for got, src in ((gk[l, b, o], kb), (gv[l, b, o], vb)):
+                # stores race per 16-byte vector: each piece is one token's
+                pieces = got.reshape(-1, 8)
+                cands = np.stack([src[l, t].reshape(-1, 8) for t in toks])
+                assert (cands == pieces[None]).all(axis=2).any(axis=0).all()
+            ek[l, b, o], ev[l, b, o] = gk[l, b, o], gv[l, b, o]
+    assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
+
+
+def _fused(kind, w, lay, key, val, kc, vc, e):
+    qsl, pos = cuda(w.qsl), cuda(w.positions)
+    if kind == "paged":
+        return kv.kv_slot_mapping_paged_write(qsl, pos, cuda(lay.table), w.block_size,
+                                              w.num_blocks, key, val, kc, vc,
+                                              max_num_tokens=w.max_num_tokens, err=e)
+    return kv.kv_slot_mapping_range_write(qsl, pos, cuda(lay.range_start), cuda(lay.range_len),
+                                          cuda(lay.num_ranges), w.block_size, w.num_blocks,
+                                          key, val, kc, vc, max_num_tokens=w.max_num_tokens,
+                                          err=e)
+
+
+@pytest.mark.parametrize("kind", ["paged", "range"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "mixed"])
+def test_fused_full_configs(name, kind):
+    if name == "mixed":
+        need = 2 * 32 * 49152 * 16 * 2048 + (8 << 30)
+        w = (wl.mixed() if free_bytes() >= need
+             else wl.mixed(num_blocks=32768, decode_ctx_max=2048))
+    else:
+        w = wl.CONFIGS[name]()
+    lay = w.layouts["G"]
+    T, B, L, H, D, E = (w.block_size, w.num_blocks, w.num_layers, w.num_kv_heads, w.head_dim,
+                        w.row_elems)
+    exp, exp_e = oracle.slot_mapping_paged(w.qsl, w.positions, lay.table, w.num_tokens,
+                                           w.max_num_tokens, T, B)
+    key = wl.bf16_normal((L, w.num_tokens, H, D), 501, dev())
+    val = wl.bf16_normal((L, w.num_tokens, H, D), 502, dev())
+    kc, vc = filled_cache((L, B, T, H, D)), filled_cache((L, B, T, H, D))
+    e = err_word()
+    slot = _fused(kind, w, lay, key, val, kc, vc, e)
+    assert int(e.item()) == exp_e == 0
+    assert np.array_equal(slot.cpu().numpy(), exp)
+    assert check_write(key, val, kc, vc, exp, L, w.num_tokens, B, T, E,
+                       np.random.default_rng(5)) == 0

@@ -52,9 +52,10 @@ def _batch(seed, R_pad, n_max, T, B, stride):
     return R, qsl, pos, table, g0, g1
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("mode", ["graph", "prepared"])
 @pytest.mark.parametrize("bulk", [False, True])
-def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode):
+def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode, fused):
     T, B, H, D, stride, R_pad = 16, 512, 8, 128, 16, 32
     n_max = R_pad
     out_rows = R_pad * stride * T
@@ -73,10 +74,17 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode):
     v_out = torch.zeros_like(k_out)
     err = err_word()
 
+    def slot_and_write(prepare=False):
+        if fused:
+            return [kv.kv_slot_mapping_paged_write(d_qsl, d_pos, d_table, T, B, key, val, kc, vc,
+                                                   max_num_tokens=n_max, slot_mapping=slot,
+                                                   err=err, prepare=prepare)]
+        return [kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
+                                         slot_mapping=slot, err=err, prepare=prepare),
+                kv.kv_cache_write(key, val, kc, vc, slot, err=err, prepare=prepare)]
+
     def step():
-        kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
-                                 slot_mapping=slot, err=err)
-        kv.kv_cache_write(key, val, kc, vc, slot, err=err)
+        slot_and_write()
         kv.kv_cache_gather(kc, vc, d_table, d_g0, d_g1, k_out=k_out, v_out=v_out,
                            out_rows=out_rows, err=err, bulk=bulk)
 
@@ -92,15 +100,13 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode):
             step()
         replay = graph.replay
     else:
-        calls = [
-            kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
-                                     slot_mapping=slot, err=err, prepare=True),
-            kv.kv_cache_write(key, val, kc, vc, slot, err=err, prepare=True),
+        calls = slot_and_write(prepare=True) + [
             kv.kv_cache_gather(kc, vc, d_table, d_g0, d_g1, k_out=k_out, v_out=v_out,
                                out_rows=out_rows, err=err, bulk=bulk, prepare=True),
         ]
         assert all(isinstance(c, kv.Prepared) for c in calls)
-        assert calls[0].result is slot and calls[2].result[0] is k_out and calls[2].result[1] is v_out
+        assert calls[0].result is slot
+        assert calls[-1].result[0] is k_out and calls[-1].result[1] is v_out
 
         def replay():  # launches on the stream current at call time
             s.wait_stream(torch.cuda.current_stream())

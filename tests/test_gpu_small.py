@@ -8,7 +8,7 @@ import torch
 import oracle
 import paged_kv_cache_39_gb300 as kv
 from paged_kv_cache_39_gb300 import workloads as wl
-from gpu_helpers import bits, cuda, dev, err_word
+from gpu_helpers import bits, cuda, dev, err_word, random_slot_case
 
 pytestmark = pytest.mark.gpu
 
@@ -132,26 +132,6 @@ def test_tiny_whole_path(layout):
 
 
 # --------------------------------------------------- adversarial slot maps
-
-
-def random_slot_case(rng):
-    T = int(rng.choice([1, 4, 16, 32]))
-    R = int(rng.integers(0, 40))
-    lens = rng.integers(0, 70, size=R)
-    lens[rng.random(R) < 0.2] = 0
-    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-    shift = int(rng.choice([0, 0, 0, 3]))
-    q = q + shift
-    N = int(q[-1]) + int(rng.choice([0, 0, 5]))
-    if rng.random() < 0.1 and R > 0:
-        q[-1] = max(q[-2], q[-1] - 2)
-    n_max = N + int(rng.choice([0, 1, 300]))
-    stride = int(rng.choice([0, 1, 8, 64]))
-    B = int(rng.integers(1, 300))
-    table = rng.integers(-1, B + 3, size=(max(R, 1), stride)).astype(np.int32)
-    table[rng.random(table.shape) < 0.2] = 0
-    pos = rng.integers(-2, max(stride, 1) * T + 20, size=N).astype(np.int64)
-    return T, R, q.astype(np.int32), N, n_max, stride, B, table, pos
 
 
 # Batches that fit one wave of CTAs run one token per thread; padding
