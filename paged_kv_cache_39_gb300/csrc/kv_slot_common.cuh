@@ -25,12 +25,23 @@ struct SlotArgs {
 };
 
 // Stage query_start_loc in shared memory when it fits; validate it grid-wide.
+// `overlap()` runs once the thread's first staging load is in flight and
+// before the barrier: work that waits on other loads (a position) can then
+// issue its own loads without holding the staging back.
+template <class Overlap>
 __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
-                                                    bool staged, uint32_t& err) {
+                                                    bool staged, uint32_t& err,
+                                                    Overlap&& overlap) {
   const int n = a.num_reqs;
   if (staged) {
-    for (int i = threadIdx.x; i <= n; i += blockDim.x) s_qsl[i] = a.qsl[i];
+    const int i0 = threadIdx.x;
+    const int32_t v0 = i0 <= n ? a.qsl[i0] : 0;
+    overlap();
+    if (i0 <= n) s_qsl[i0] = v0;
+    for (int i = i0 + blockDim.x; i <= n; i += blockDim.x) s_qsl[i] = a.qsl[i];
     __syncthreads();
+  } else {
+    overlap();
   }
   const int32_t* q = staged ? s_qsl : a.qsl;
   if (n > 0) {
@@ -40,6 +51,11 @@ __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* 
       err |= KV_ERR_BAD_QSL;
   }
   return q;
+}
+
+__device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
+                                                    bool staged, uint32_t& err) {
+  return stage_qsl(a, s_qsl, staged, err, [] {});
 }
 
 // Request owning token t (t < num_tokens), or -1 when no span covers it.

@@ -42,39 +42,59 @@ struct RowArgs {
 };
 
 // Block of logical block lb of request r through the block table (kNull
-// when the row has no entry there).  Warp-uniform arguments.
+// when the row has no entry there).  The lookup is split in two: prefetch()
+// issues the loads of request r's row, resolve() consumes them, so the loads
+// can be started before the request is known for sure.  Warp-uniform
+// arguments.
 struct PagedLookup {
   const int32_t* __restrict__ table;
   int32_t stride;
   static constexpr bool kRows = false;
-  __device__ __forceinline__ int64_t block(int r, int64_t lb) const {
-    return lb < stride ? (int64_t)table[(int64_t)r * stride + lb] : (int64_t)kNull;
+  static constexpr bool kNeedsBlock = true;  // prefetch() reads the entry of lb
+  struct Pre {
+    int32_t entry;
+  };
+  __device__ __forceinline__ Pre prefetch(int r, int64_t lb) const {
+    return Pre{lb < stride ? table[(int64_t)r * stride + lb] : kNull};
+  }
+  __device__ __forceinline__ int64_t resolve(const Pre& pre, int, int64_t) const {
+    return pre.entry;
   }
 };
 
 // The same through range descriptors: range i covers logical blocks
-// [cum_i, cum_i + len_i) from physical block start_i.  Every lane of the warp
-// calls it with the same (r, lb).  Lengths below zero count as zero and a
-// count outside [0, stride] resolves nothing (both are reported by the row
-// sweep), as in the range slot map.
+// [cum_i, cum_i + len_i) from physical block start_i.  The prefetch is the
+// row's descriptors 0..31 (one per lane) and its count; the rest of a row
+// with more than 32 ranges is read 32 at a time while resolving.  Lengths
+// below zero count as zero and a count outside [0, stride] resolves nothing
+// (both are reported by the row sweep), as in the range slot map.
 struct RangeLookup {
   const int32_t* __restrict__ start;
   const int32_t* __restrict__ len;
   const int32_t* __restrict__ count;
   int32_t stride;
   static constexpr bool kRows = true;
-  __device__ __forceinline__ int64_t block(int r, int64_t lb) const {
+  static constexpr bool kNeedsBlock = false;  // prefetch() reads the row's head
+  struct Pre {
+    int32_t s, l, nr;
+  };
+  __device__ __forceinline__ Pre prefetch(int r, int64_t) const {
     const int lane = threadIdx.x & 31;
+    Pre pre{0, 0, 0};
+    if (lane < stride) {
+      pre.s = start[(int64_t)r * stride + lane];
+      pre.l = len[(int64_t)r * stride + lane];
+    }
+    pre.nr = count[r];
+    return pre;
+  }
+  __device__ __forceinline__ int64_t resolve(const Pre& pre, int r, int64_t lb) const {
+    const int lane = threadIdx.x & 31;
+    const int32_t nr = pre.nr;
+    if (nr < 0 || nr > stride) return kNull;
     const int32_t* rs = start + (int64_t)r * stride;
     const int32_t* rl = len + (int64_t)r * stride;
-    // descriptors 0..31 are requested together with the count
-    int32_t s = 0, l = 0;
-    if (lane < stride) {
-      s = rs[lane];
-      l = rl[lane];
-    }
-    const int32_t nr = count[r];
-    if (nr < 0 || nr > stride) return kNull;
+    int32_t s = pre.s, l = pre.l;
     int64_t cum = 0;
     for (int c0 = 0; c0 < nr; c0 += 32) {
       const int i = c0 + lane;
@@ -157,6 +177,18 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
       }
     }
   }
+  // A decode batch gives request t its token t (one token each): request t's
+  // row is requested before query_start_loc says whose token t is, and used
+  // if the lookup below confirms the guess.  A wrong guess (t inside a longer
+  // request) only costs the unused loads.  The range row needs no position
+  // and goes out at once; the table entry waits on the position and goes out
+  // while query_start_loc is being staged.
+  const bool guess = live && t < a.num_reqs;
+  int64_t lb = 0, off = 0;
+  typename Lookup::Pre g_pre{};
+  if constexpr (!Lookup::kNeedsBlock) {
+    if (guess) g_pre = lk.prefetch(t, 0);
+  }
   uint32_t err = 0;
   // descriptor-row validation, one row per thread grid-wide (range form): the
   // first row is requested now and checked at the end
@@ -165,18 +197,22 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   if constexpr (Lookup::kRows) {
     if (sweep0 < a.num_reqs) first_row.load(lk.count, lk.len, sweep0, lk.stride, vec4);
   }
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err, [&] {
+    if (live && p >= 0) a.bs.divmod(p, lb, off);
+    if constexpr (Lookup::kNeedsBlock) {
+      if (guess && p >= 0) g_pre = lk.prefetch(t, lb);
+    }
+  });
 
-  int64_t b = kNull, off = 0, slot = kPad;
+  int64_t b = kNull, slot = kPad;
   if (live) {
     const int r = request_of(q, a.num_reqs, t);
     if (r >= 0) {
       if (p < 0) {
         err |= KV_ERR_BAD_POSITION;
       } else {
-        int64_t lb;
-        a.bs.divmod(p, lb, off);
-        b = lk.block(r, lb);
+        const typename Lookup::Pre pre = (guess && r == t) ? g_pre : lk.prefetch(r, lb);
+        b = lk.resolve(pre, r, lb);
         slot = slot_of(b, off, a.bs.size, a.num_blocks, err);
       }
     }

@@ -136,3 +136,45 @@ def test_fused_full_configs(name, kind):
     assert np.array_equal(slot.cpu().numpy(), exp)
     assert check_write(key, val, kc, vc, exp, L, w.num_tokens, B, T, E,
                        np.random.default_rng(5)) == 0
+
+
+@pytest.mark.parametrize("kind", ["paged", "range"])
+@pytest.mark.parametrize("R", [2047, 2048, 6000])
+def test_fused_many_requests(R, kind):
+    """Up to 2047 requests the CTA stages query_start_loc in shared memory;
+    past that each warp searches it in global memory."""
+    rng = np.random.default_rng(7500 + R)
+    T, H, D, stride = 16, 1, 64, 4
+    lens = rng.integers(0, 3, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    B = R * stride + 1
+    table = rng.permutation(np.arange(1, B)).astype(np.int32)[:R * stride].reshape(R, stride)
+    # distinct positions within a request, so no two tokens share a slot
+    pos = np.concatenate([rng.choice(stride * T + 8, size=n, replace=False)
+                          for n in lens]).astype(np.int64)
+    rs, rl = table[:, :1].copy(), np.ones((R, 1), np.int32)  # one single-block range per row
+    nr = np.ones(R, np.int32)
+    if kind == "paged":
+        exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N + 5, T, B)
+    else:
+        exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N + 5, T, B)
+    key = wl.bf16_normal((1, N, H, D), 7600 + R)
+    val = wl.bf16_normal((1, N, H, D), 7700 + R)
+    kc = torch.zeros((1, B, T, H, D), dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    assert oracle.cache_write(bits(key), bits(val), ek, ev, exp_s[:N], B, T) == 0
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    if kind == "paged":
+        s = kv.kv_slot_mapping_paged_write(cuda(q), cuda(pos), cuda(table), T, B, key.to(dev()),
+                                           val.to(dev()), kc_d, vc_d, max_num_tokens=N + 5,
+                                           err=e)
+    else:
+        s = kv.kv_slot_mapping_range_write(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T,
+                                           B, key.to(dev()), val.to(dev()), kc_d, vc_d,
+                                           max_num_tokens=N + 5, err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(s.cpu().numpy(), exp_s)
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
