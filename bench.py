@@ -527,10 +527,12 @@ BUILDERS = {"decode": build_decode, "mixed": build_mixed, "long": build_long,
 def flush_l2(buf):
     """Write a buffer larger than L2, then read another one: the read evicts the
     dirty lines the write left, so their write-back happens here and not
-    inside the next timed step."""
+    inside the next timed step.  The read is an int32 max (a sum would first
+    cast the half to int64 through a freshly written temporary, leaving L2
+    dirty again)."""
     n = buf.numel() // 2
     buf[:n].add_(1)
-    buf[n:].sum()
+    buf[n:].max()
 
 
 def time_steps(torch, built, steps, flush_buf, stream):
