@@ -146,7 +146,8 @@ def kernel_source_sha(kernel: str) -> str:
              "table_from_ranges_kernel": "kv_range_table.cu",
              "copy_blocks_kernel": "kv_copy_blocks.cu",
              "cache_gather_bulk_kernel": "kv_cache_gather.cu",
-             "slot_write_kernel": "kv_slot_write.cu"}
+             "slot_write_kernel": "kv_slot_write.cu",
+             "copy_blocks_bulk_kernel": "kv_copy_blocks.cu"}
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc")
     for f in [files[kernel]] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
@@ -345,6 +346,9 @@ def build_mixed(torch, kv, wl, dev, small=False):
         Launch("copy_blocks[cow 1024]", "copy_blocks_kernel",
                lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err),
                n_cow * L * T * w.row_bytes * 4 + n_cow * 8, n_cow * L),
+        Launch("copy_blocks_bulk[cow 1024]", "copy_blocks_bulk_kernel",
+               lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err, bulk=True),
+               n_cow * L * T * w.row_bytes * 4 + n_cow * 8, n_cow * L),
     ]
     desc = (f"mixed prefill+decode: 16 prefill chunks (8192 tokens) + 240 decode tokens, "
             f"{L} layers, {B}-block pool per layer, KV 8x128 bf16, 1-8 ranges/request{note}")
@@ -416,6 +420,9 @@ def build_long(torch, kv, wl, dev, small=False):
                lg.table.size * 4 + int(lg.num_ranges.sum()) * 8 + R * 4, R),
         Launch(f"copy_blocks[cow {n_cow}]", "copy_blocks_kernel",
                lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err),
+               n_cow * T * w.row_bytes * 4 + n_cow * 8, n_cow),
+        Launch(f"copy_blocks_bulk[cow {n_cow}]", "copy_blocks_bulk_kernel",
+               lambda: kv.kv_copy_blocks(kc, vc, cow_src, cow_dst, err=err, bulk=True),
                n_cow * T * w.row_bytes * 4 + n_cow * 8, n_cow),
     ]
     desc = (f"long-context gather: {R} requests x 131072 tokens, block_size 16, KV 8x128 bf16; "

@@ -1,7 +1,7 @@
 /*
  * kvpaged.h -- C ABI of the GB300 paged KV-cache hot path (libkvpaged.so).
  *
- * Twelve calls, each one kernel launch on the caller's stream:
+ * Thirteen calls, each one kernel launch on the caller's stream:
  *   kv_slot_mapping_paged    token -> cache slot through a block table
  *   kv_slot_mapping_paged_cp the same, for one rank of context parallelism
  *   kv_slot_mapping_range    token -> cache slot through contiguous ranges
@@ -14,6 +14,7 @@
  *   kv_table_from_ranges     range descriptors -> block table
  *   kv_cache_gather_range    the gather, with blocks found from ranges
  *   kv_copy_blocks           copy-on-write copy of whole blocks
+ *   kv_copy_blocks_bulk      the same copies, moved by bulk (TMA) copies
  *
  * Sources (page title, section):
  *   [BT]  "Blocktabelle" (vLLM v0.25.1 walkthrough)
@@ -420,6 +421,21 @@ int kv_copy_blocks(void* k_cache, void* v_cache, int32_t num_layers, int64_t num
                    int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                    const int32_t* src_blocks, const int32_t* dst_blocks, int32_t num_pairs,
                    int32_t* d_err, kv_stream_t stream);
+
+/*
+ * kv_copy_blocks_bulk -- kv_copy_blocks moved by the bulk-copy (TMA) engine.
+ *
+ * The same arguments, results, error bits and rules as kv_copy_blocks.  Each
+ * K or V block of a (pair, layer) -- or each 32 KiB piece of a larger block --
+ * goes global -> shared -> global with cp.async.bulk from one thread per
+ * one-warp CTA, two CTAs per SM.  Every wait on the copy engine is bounded:
+ * one that runs out sets KV_ERR_TIMEOUT and the kernel ends normally.
+ * Errors: as kv_copy_blocks; KV_ECUDA if the shared-memory size cannot be set.
+ */
+int kv_copy_blocks_bulk(void* k_cache, void* v_cache, int32_t num_layers, int64_t num_blocks,
+                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                        const int32_t* src_blocks, const int32_t* dst_blocks,
+                        int32_t num_pairs, int32_t* d_err, kv_stream_t stream);
 
 /*
  * kv_diag_bounded_wait -- self-test of the bounded wait the bulk-copy gather

@@ -55,6 +55,8 @@ SIGNATURES = {
     "kv_cache_gather_range": ([_P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _P, _P, _I32, _P, _P,
                                _I32, _P, _P, _I64, _P, _P], ctypes.c_int),
     "kv_copy_blocks": ([_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P], ctypes.c_int),
+    "kv_copy_blocks_bulk": ([_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _I32, _P, _P],
+                            ctypes.c_int),
     "kv_diag_bounded_wait": ([_I32, _P, _P], ctypes.c_int),
     "kv_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "kv_abi_version": ([], ctypes.c_int),

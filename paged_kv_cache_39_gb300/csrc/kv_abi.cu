@@ -57,4 +57,4 @@ extern "C" const char* kv_status_string(int status) {
   }
 }
 
-extern "C" int kv_abi_version(void) { return 6; }
+extern "C" int kv_abi_version(void) { return 7; }

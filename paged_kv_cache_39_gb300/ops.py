@@ -417,9 +417,10 @@ def kv_cache_gather_range(k_cache: torch.Tensor, v_cache: torch.Tensor,
 
 def kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: torch.Tensor,
                    dst_blocks: torch.Tensor, err: Optional[torch.Tensor] = None,
-                   prepare: bool = False):
+                   bulk: bool = False, prepare: bool = False):
     """Copy whole blocks src -> dst (every layer, K and V) in place.
 
+    ``bulk=True`` calls kv_copy_blocks_bulk (bulk-copy engine) instead.
     Returns None (or the ``Prepared`` call)."""
     dev = _device_of(k_cache, "k_cache")
     L, B, T, H, D = _cache_dims(k_cache, v_cache, dev)
@@ -429,5 +430,5 @@ def kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_blocks: tor
         raise ValueError("src_blocks and dst_blocks differ in length")
     args = (_ptr(k_cache), _ptr(v_cache), L, B, T, H, D, _ptr(src_blocks), _ptr(dst_blocks),
             src_blocks.numel(), _err_ptr(err, dev))
-    return _run("kv_copy_blocks", args, dev, (k_cache, v_cache, src_blocks, dst_blocks, err),
-                None, prepare)
+    return _run("kv_copy_blocks_bulk" if bulk else "kv_copy_blocks", args, dev,
+                (k_cache, v_cache, src_blocks, dst_blocks, err), None, prepare)

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kv_abi_version() == 6
+    assert lib.kv_abi_version() == 7
     assert lib.kv_status_string(0) == b"KV_OK"
     assert b"EINVAL" in lib.kv_status_string(-1)
     assert b"EUNSUPPORTED" in lib.kv_status_string(-2)
@@ -128,6 +128,13 @@ def test_next_step_calls_reject_bad_arguments(lib):
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 1, N, N) == -1
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, 0, N, N) == 0
     assert lib.kv_copy_blocks(N, N, 1, 8, 16, 8, 64, N, N, -1, N, N) == -1
+    # kv_copy_blocks_bulk: the same checks
+    assert lib.kv_copy_blocks_bulk(N, N, 1, 8, 16, 3, 5, N, N, 1, N, N) == -2
+    assert lib.kv_copy_blocks_bulk(N, N, 1, 8, 16, 8, 64, N, N, 1, N, N) == -1
+    assert lib.kv_copy_blocks_bulk(N, N, 1, 8, 16, 8, 64, N, N, 0, N, N) == 0
+    assert lib.kv_copy_blocks_bulk(N, N, 1, 8, 16, 8, 64, N, N, -1, N, N) == -1
+    assert lib.kv_copy_blocks_bulk(0x1008, 0x2000, 1, 8, 16, 8, 64, 0x3000, 0x4000, 1, N,
+                                   N) == -1  # misaligned cache
 
 
 def test_cp_slot_mapping_rejects_bad_arguments(lib):

@@ -139,8 +139,9 @@ def test_gather_range_equals_table_gather_full_size(name):
 # ------------------------------------------------------- copy-on-write
 
 
+@pytest.mark.parametrize("bulk", [False, True])
 @pytest.mark.parametrize("L,H,D", [(1, 8, 128), (3, 8, 64), (2, 16, 128), (2, 1, 128), (0, 8, 64)])
-def test_copy_blocks_parity(L, H, D):
+def test_copy_blocks_parity(L, H, D, bulk):
     rng = np.random.default_rng(9200 + L * 7 + H + D)
     B, T, P = 64, 16, 20
     perm = rng.permutation(np.arange(1, B))
@@ -156,7 +157,28 @@ def test_copy_blocks_parity(L, H, D):
     exp_e = oracle.copy_blocks(ek, ev, src, dst)
     kc_d, vc_d = kc.to(dev()), vc.to(dev())
     e = err_word()
-    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e)
+    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e, bulk=bulk)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+
+
+@pytest.mark.parametrize("T,H,D", [(12, 16, 128), (16, 32, 128), (3, 1, 8), (1, 8, 128)])
+def test_copy_blocks_bulk_piece_sizes(T, H, D):
+    """Blocks of 48 KiB and 128 KiB move as 32 KiB pieces plus a remainder;
+    tiny blocks (48 B, 2 KiB) as one piece each."""
+    rng = np.random.default_rng(9250 + T + H + D)
+    L, B, P = 2, 40, 12
+    perm = rng.permutation(np.arange(1, B))
+    src = perm[:P].astype(np.int32)
+    dst = perm[P:2 * P].astype(np.int32)
+    src[2], dst[4] = 0, B  # a null source, an out-of-range destination
+    kc = wl.bf16_normal((L, B, T, H, D), 300 + T)
+    vc = wl.bf16_normal((L, B, T, H, D), 310 + T)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_e = oracle.copy_blocks(ek, ev, src, dst)
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e, bulk=True)
     assert int(e.item()) == exp_e
     assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
 
@@ -178,8 +200,9 @@ def test_copy_then_write_diverges_only_the_copy():
     assert torch.equal(same, exp)
 
 
+@pytest.mark.parametrize("bulk", [False, True])
 @pytest.mark.parametrize("P,L,T", [(1000, 3, 16), (2000, 4, 6)])
-def test_copy_blocks_grouped_path(P, L, T):
+def test_copy_blocks_grouped_path(P, L, T, bulk):
     """Batches of tens of thousands of rows copy four rows per warp step; a
     block size of 6 leaves a two-row remainder in every block."""
     rng = np.random.default_rng(9300 + P + T)
@@ -194,6 +217,6 @@ def test_copy_blocks_grouped_path(P, L, T):
     exp_e = oracle.copy_blocks(ek, ev, src, dst)
     kc_d, vc_d = kc.to(dev()), vc.to(dev())
     e = err_word()
-    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e)
+    kv.kv_copy_blocks(kc_d, vc_d, cuda(src), cuda(dst), err=e, bulk=bulk)
     assert int(e.item()) == exp_e
     assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
