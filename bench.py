@@ -27,6 +27,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -138,7 +139,8 @@ class ClockSampler:
 
 
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of the sources a kernel is built from (its .cu file and the headers)."""
+    """Hash of the sources a kernel is built from (its .cu file and the
+    library headers it includes)."""
     files = {"cache_gather_kernel": "kv_cache_gather.cu", "cache_write_kernel": "kv_cache_write.cu",
              "slot_mapping_paged_kernel": "kv_slot_mapping.cu",
              "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu",
@@ -148,10 +150,19 @@ def kernel_source_sha(kernel: str) -> str:
              "cache_gather_bulk_kernel": "kv_cache_gather.cu",
              "slot_write_kernel": "kv_slot_write.cu",
              "copy_blocks_bulk_kernel": "kv_copy_blocks.cu"}
-    h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc")
-    for f in [files[kernel]] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
-        with open(os.path.join(ROOT, "paged_kv_cache_39_gb300", "csrc", f), "rb") as fh:
+    # the .cu file and, recursively, the library headers it includes
+    order, todo = [], [files[kernel]]
+    while todo:
+        f = todo.pop(0)
+        if f in order or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        order.append(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo += re.findall(r'^#include "([^"]+)"', fh.read(), flags=re.M)
+    h = hashlib.sha256()
+    for f in order:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
