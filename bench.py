@@ -29,7 +29,6 @@ import json
 import os
 import re
 import statistics
-import subprocess
 import sys
 import threading
 import time

@@ -1,7 +1,6 @@
 """CPU-side checks of the C ABI: the library loads, exports every symbol the
 header declares, and rejects invalid host-visible arguments before launching
 anything (these calls never reach the GPU)."""
-import ctypes
 import os
 import re
 

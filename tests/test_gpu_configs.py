@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_kv_cache_39_gb300 as kv
 from paged_kv_cache_39_gb300 import workloads as wl
-from gpu_helpers import (FILL, SAMPLE, bits, check_write, cuda, dev, device_rows_equal, err_word,
+from gpu_helpers import (FILL, SAMPLE, check_write, cuda, dev, device_rows_equal, err_word,
                          filled_cache, free_bytes, rows_view, sample_host_check)
 
 pytestmark = pytest.mark.gpu
