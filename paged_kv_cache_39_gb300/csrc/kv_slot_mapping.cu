@@ -12,10 +12,10 @@
 // fixed tile of 256 x TPT consecutive tokens (TPT per thread, coalesced, all
 // of a thread's loads in flight together), so the grid depends only on
 // max_num_tokens (stable under CUDA-graph capture) and long prefills spread
-// over every SM.  TPT is 1 while one token per thread fits in one wave of
-// resident CTAs (up to ~155K tokens on 152 SMs: the shortest dependency chain
-// per thread, measured 1.2-6 us faster on decode and mixed batches), then
-// grows through 4, 8 and 16 so that the grid stays within about one wave.
+// over every SM.  TPT is 1 for batches up to a few hundred thousand tokens
+// (the shortest dependency chain per thread, measured 1.2-6 us faster on
+// decode and mixed batches than 4), then 4 (paged) or 4-8 (range); the
+// thresholds were measured per map (see the *_tokens_per_thread rules).
 // Each thread finds its request by a binary search of query_start_loc staged
 // in shared memory.  The tail [num_tokens, max_num_tokens) is just more tiles
 // that store PAD.
@@ -385,14 +385,23 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   report(a.err, err);
 }
 
-// Tokens per thread: 1 while that grid fits one wave (4 resident CTAs per
-// SM), else the smallest of 4, 8, 16 that keeps the grid within about one wave.
-int tokens_per_thread(int32_t max_num_tokens) {
+// Tokens per thread, measured per map (ncu, cold caches, 262K-2.6M
+// positions).  A wave is 4 resident CTAs per SM.
+// Paged map: 1 while the grid is at most two waves (~311K tokens), else 4
+// (4 beat 8 and 16 at every size: 7.1 vs 7.5 / 9.1 us at 1M positions,
+// 11.6 vs 13.5 / 18.8 us at 2.6M).
+int paged_tokens_per_thread(int32_t max_num_tokens) {
+  const int64_t wave = (int64_t)sm_count() * 4;
+  return ((int64_t)max_num_tokens + kThreads - 1) / kThreads <= 2 * wave ? 1 : 4;
+}
+
+// Range map: 1 while the grid fits one wave, else the smaller of 4 and 8
+// that keeps the grid within about one wave (its per-token state is larger,
+// and at 1M-2.6M positions 8 was level with or ahead of 4).
+int range_tokens_per_thread(int32_t max_num_tokens) {
   const int64_t wave = (int64_t)sm_count() * 4;
   if (((int64_t)max_num_tokens + kThreads - 1) / kThreads <= wave) return 1;
-  for (int tpt = 4; tpt < 16; tpt *= 2)
-    if (((int64_t)max_num_tokens + kThreads * tpt - 1) / (kThreads * tpt) <= wave) return tpt;
-  return 16;
+  return ((int64_t)max_num_tokens + kThreads * 4 - 1) / (kThreads * 4) <= wave ? 4 : 8;
 }
 
 int grid_for(int32_t max_num_tokens, int tpt) {
@@ -414,7 +423,7 @@ int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
     return KV_EINVAL;
   if (d_err != nullptr && !aligned(d_err, 4)) return KV_EINVAL;
   if (max_num_tokens == 0 && num_reqs == 0) return KV_OK;
-  const int tpt = tokens_per_thread(max_num_tokens);
+  const int tpt = paged_tokens_per_thread(max_num_tokens);
   const int grid = grid_for(max_num_tokens, tpt);
   const bool staged = num_reqs + 1 <= kQslSmemMax;
   const size_t smem = staged && num_reqs > 0 ? sizeof(int32_t) * (num_reqs + 1) : 0;
@@ -424,15 +433,9 @@ int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
   if (tpt == 1)
     slot_mapping_paged_kernel<1, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
                                                                           table_stride, st, cp);
-  else if (tpt == 4)
+  else
     slot_mapping_paged_kernel<4, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
                                                                           table_stride, st, cp);
-  else if (tpt == 8)
-    slot_mapping_paged_kernel<8, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                          table_stride, st, cp);
-  else
-    slot_mapping_paged_kernel<16, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                           table_stride, st, cp);
   return launch_status();
 }
 
@@ -499,8 +502,7 @@ extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64
   if (rc != KV_OK) return rc;
   if (d_err != nullptr && !aligned(d_err, 4)) return KV_EINVAL;
   if (max_num_tokens == 0 && num_reqs == 0) return KV_OK;
-  // the range kernel's per-token state is larger: at most 8 tokens per thread
-  const int tpt = min(8, tokens_per_thread(max_num_tokens));
+  const int tpt = range_tokens_per_thread(max_num_tokens);
   const int grid = grid_for(max_num_tokens, tpt);
   const bool staged = num_reqs + 1 <= kQslSmemMax;
   const size_t smem = staged && num_reqs > 0 ? sizeof(int32_t) * (num_reqs + 1) : 0;

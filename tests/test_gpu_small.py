@@ -134,10 +134,11 @@ def test_tiny_whole_path(layout):
 # --------------------------------------------------- adversarial slot maps
 
 
-# Batches that fit one wave of CTAs run one token per thread; padding
-# max_num_tokens past that (200k) makes the same tokens run 4 per thread, with
-# the lane windows and warp descriptor cache carried across a thread's tokens.
-PADS = [0, 200_000]
+# Batches of up to a few hundred thousand tokens run one token per thread;
+# padding max_num_tokens to 400k makes the same tokens run 4 per thread in
+# both maps, with the range map's lane windows and warp descriptor cache
+# carried across a thread's tokens.
+PADS = [0, 400_000]
 
 
 @pytest.mark.parametrize("pad", PADS)
@@ -346,8 +347,8 @@ def test_expand_random_parity(k, extra):
 
 @pytest.mark.parametrize("n_max", [1000, 150_000, 400_000, 700_000, 1_300_000, 2_600_000])
 def test_slot_mapping_tile_variants(n_max):
-    """Batches past one wave of CTAs switch to 4, 8 and 16 tokens per thread;
-    results are unchanged."""
+    """Larger batches switch to 4 tokens per thread (paged) and 4, then 8
+    (range); results are unchanged."""
     rng = np.random.default_rng(n_max)
     T, R = 16, 37
     lens = rng.multinomial(n_max - 5, np.ones(R) / R)
