@@ -62,7 +62,7 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
   // phase 1: table index of every token of the thread (-1: PAD without lookup)
   int64_t idx[kTokPerThread], off[kTokPerThread];
-  int last_r = -1;
+  ReqSpan last_r;
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
@@ -281,7 +281,7 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, sweep0, rstride, vec4);
 
   RangeWindow win;  // this lane's last resolved range
-  int last_r = -1;
+  ReqSpan last_r;
 #pragma unroll 1
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
