@@ -178,3 +178,40 @@ def test_fused_many_requests(R, kind):
     assert int(e.item()) == exp_e
     assert np.array_equal(s.cpu().numpy(), exp_s)
     assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_row_check_covers_rows_past_the_grid(fused):
+    """A batch of 1000 descriptor rows and only 16 tokens runs on one CTA
+    (256 threads, or 2 CTAs for the fused call): the grid-wide row check
+    must still loop over every row and flag the malformed ones."""
+    rng = np.random.default_rng(7900)
+    R, T, B, S = 1000, 16, 5000, 4
+    rs = rng.permutation(np.arange(1, B))[:R * S].reshape(R, S).astype(np.int32)  # distinct
+    rl = np.ones((R, S), np.int32)
+    nr = rng.integers(1, S + 1, size=R).astype(np.int32)
+    nr[300] = S + 2                   # count above the stride
+    rl[999, 0] = 0                    # zero-length first range
+    nr[999] = max(nr[999], 1)
+    lens = np.zeros(R, np.int64)
+    lens[[0, 5, 700]] = [6, 6, 4]
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    pos = np.concatenate([np.arange(n) for n in lens]).astype(np.int64)
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+    assert exp_e == kv.ERR_BITS["BAD_RANGE"]
+    e = err_word()
+    if fused:
+        H, D = 1, 8
+        key = wl.bf16_normal((1, N, H, D), 7901)
+        kc = torch.zeros((1, B, T, H, D), dtype=torch.bfloat16)
+        ek, ev = bits(kc).copy(), bits(kc).copy()
+        oracle.cache_write(bits(key), bits(key), ek, ev, exp_s, B, T)
+        kc_d, vc_d = kc.to(dev()), kc.clone().to(dev())
+        s = kv.kv_slot_mapping_range_write(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B,
+                                           key.to(dev()), key.to(dev()), kc_d, vc_d, err=e)
+        assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+    else:
+        s = kv.kv_slot_mapping_range(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B, err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(s.cpu().numpy(), exp_s)
