@@ -215,3 +215,34 @@ def test_row_check_covers_rows_past_the_grid(fused):
         s = kv.kv_slot_mapping_range(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B, err=e)
     assert int(e.item()) == exp_e
     assert np.array_equal(s.cpu().numpy(), exp_s)
+
+
+@pytest.mark.parametrize("call", ["paged", "range", "paged_write"])
+def test_qsl_check_covers_entries_past_the_grid(call):
+    """query_start_loc decreasing at entry 2500 of 3000, with 16 tokens (one
+    or two CTAs): the grid-wide check still reaches it and sets BAD_QSL."""
+    R, T, B, S = 3000, 16, 4000, 4
+    lens = np.zeros(R, np.int64)
+    lens[[1, 2]] = [10, 6]
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q[2500] = q[2501] + 1  # decreasing once
+    N = 16
+    pos = np.arange(N, dtype=np.int64)
+    table = np.arange(1, R * S + 1, dtype=np.int32).reshape(R, S) % (B - 1) + 1
+    rs, rl, nr = table[:, :1].copy(), np.ones((R, 1), np.int32), np.ones(R, np.int32)
+    _, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N, T, B)
+    assert exp_e & kv.ERR_BITS["BAD_QSL"]
+    e = err_word()
+    if call == "paged":
+        kv.kv_slot_mapping_paged(cuda(q), cuda(pos), cuda(table), T, B, err=e)
+    elif call == "range":
+        _, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+        kv.kv_slot_mapping_range(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B, err=e)
+    else:
+        key = torch.zeros((1, N, 1, 8), dtype=torch.bfloat16, device=dev())
+        kc = torch.zeros((1, B, T, 1, 8), dtype=torch.bfloat16, device=dev())
+        kv.kv_slot_mapping_paged_write(cuda(q), cuda(pos), cuda(table), T, B, key, key, kc,
+                                       kc.clone(), err=e)
+    # slot values are unspecified under a bad qsl; the error word is not
+    assert int(e.item()) & kv.ERR_BITS["BAD_QSL"]
+    assert int(e.item()) == exp_e
