@@ -1086,7 +1086,19 @@ def main():
             stream, peak)
         line["gather_GBps"] = kernels["cache_gather"]["GB/s"]
         line["graph"] = graph_decode(torch, built, min(args.steps, 500), flush_buf)
-        line["e2e"] = e2e_decode(torch, kv, built, min(args.steps, 1000), flush_buf, stream)
+        if rk.world_size > 1:
+            g_ms = kdist.max_over_ranks(line["graph"]["ms_per_step"], dev)
+            line["graph"]["ms_per_step"] = round(g_ms, 4)
+            line["graph"]["value"] = round(built.tokens * rk.world_size / (g_ms * 1e-3), 1)
+        e2e = e2e_decode(torch, kv, built, min(args.steps, 1000), flush_buf, stream)
+        if rk.world_size > 1:
+            # whole job, like `value`: every rank's tokens over the slowest rank's step
+            kdist.barrier(dev)
+            e2e_ms = kdist.max_over_ranks(e2e["ms_per_step"], dev)
+            e2e["per_gpu_value"] = e2e["value"]
+            e2e["ms_per_step"] = round(e2e_ms, 4)
+            e2e["value"] = round(built.tokens * rk.world_size / (e2e_ms * 1e-3), 1)
+        line["e2e"] = e2e
 
     if rk.is_main and rk.world_size == 1:
         if args.workload == "decode" and args.cpu_seconds > 0:
