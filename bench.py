@@ -987,7 +987,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
             "note": "wall time over all steps: each step uploads its packed inputs from pinned "
                     "host memory (copy stream, double-buffered so step k+1's upload overlaps "
                     "step k), runs the four prepared calls and copies both slot mappings and "
-                    "the error word back, which the host checks one step later; "
+                    "the error word back, which the host checks one step later; steps run "
+                    "back to back without an L2 flush (each moves 4.9 GB, far more than L2); "
                     "sync_ms_per_step: median of the same step run alone and waited for, L2 "
                     "flushed before it"}
 
