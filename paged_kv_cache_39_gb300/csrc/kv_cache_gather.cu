@@ -218,6 +218,8 @@ __device__ __forceinline__ void gather_rows(const GatherArgs& a, const int64_t* 
 }
 
 __global__ void __launch_bounds__(kThreads) cache_gather_kernel(GatherArgs a) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ int64_t smem[];
   int64_t* s_off = smem;                                                 // [num_reqs + 1]
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + a.num_reqs + 1);  // [num_reqs]
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(kThreads)
 cache_gather_range_kernel(GatherArgs a, const int32_t* __restrict__ range_start,
                           const int32_t* __restrict__ range_len,
                           const int32_t* __restrict__ num_ranges, int32_t rstride) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ int64_t smem[];
   int64_t* s_off = smem;
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + a.num_reqs + 1);
@@ -280,6 +284,8 @@ __host__ __device__ constexpr size_t bulk_smem_bytes(int num_reqs) {
 }
 
 __global__ void __launch_bounds__(32) cache_gather_bulk_kernel(GatherArgs a, int32_t chunk_rows) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ __align__(128) unsigned char bulk_smem[];
   const int R = a.num_reqs;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bulk_smem);
@@ -491,8 +497,7 @@ static int launch_gather(Kernel kernel, const GatherArgs& a, Extra... extra) {
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return KV_ECUDA;
-  kernel<<<grid, kThreads, smem, a.stream>>>(a, extra...);
-  return launch_status();
+  return launch_pdl(kernel, grid, kThreads, smem, a.stream, a, extra...);
 }
 
 extern "C" int kv_cache_gather(const void* k_cache, const void* v_cache, int32_t layer,
@@ -549,8 +554,7 @@ extern "C" int kv_cache_gather_bulk(const void* k_cache, const void* v_cache, in
                            (int)smem) != cudaSuccess)
     return KV_ECUDA;
   const int grid = sm_count() * kBulkCtasPerSm;
-  cache_gather_bulk_kernel<<<grid, 32, smem, stream>>>(a, chunk_rows);
-  return launch_status();
+  return launch_pdl(cache_gather_bulk_kernel, grid, 32, smem, stream, a, chunk_rows);
 }
 
 extern "C" int kv_cache_gather_range(const void* k_cache, const void* v_cache, int32_t layer,

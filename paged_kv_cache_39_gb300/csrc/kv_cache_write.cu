@@ -71,6 +71,8 @@ cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ valu
                    const int64_t* __restrict__ slot_mapping, int32_t num_tokens,
                    int64_t items, int64_t num_blocks, int32_t block_size, int32_t row_vecs,
                    int32_t* err_word) {
+  pdl_allow_next();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -129,9 +131,8 @@ extern "C" int kv_cache_write(const void* key, const void* value, void* k_cache,
   const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);
   auto k4 = cache_write_kernel<4>;
   auto k1 = cache_write_kernel<1>;
-  (grouped ? k4 : k1)<<<grid, kThreads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
-      items, num_blocks, block_size, row_vecs, d_err);
-  return launch_status();
+  return launch_pdl(grouped ? k4 : k1, grid, kThreads, 0, stream,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
+                    num_tokens, items, num_blocks, block_size, row_vecs, d_err);
 }

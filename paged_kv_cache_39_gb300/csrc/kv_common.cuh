@@ -229,4 +229,36 @@ inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
 }
 
+// Programmatic dependent launch.  A kernel launched through launch_pdl() may
+// be scheduled while the previous kernel on the stream is still running; it
+// lets its own successor be scheduled at once (pdl_allow_next), then waits
+// for the previous grid to complete, its memory visible (pdl_wait), before
+// its first global load or store.  Results are those of plain stream order;
+// only the gap between dependent launches shrinks.  Both instructions are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = {};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KV_ECUDA;
+  }
+  return KV_OK;
+}
+
 }  // namespace kvp

@@ -29,6 +29,8 @@ copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                    int32_t row_vecs, const int32_t* __restrict__ src_blocks,
                    const int32_t* __restrict__ dst_blocks, int64_t num_pairs,
                    int32_t* err_word) {
+  pdl_allow_next();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -100,6 +102,8 @@ copy_blocks_bulk_kernel(unsigned char* __restrict__ k_cache, unsigned char* __re
                         int32_t pieces, const int32_t* __restrict__ src_blocks,
                         const int32_t* __restrict__ dst_blocks, int64_t num_pairs,
                         int32_t* err_word) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ __align__(128) unsigned char copy_smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(copy_smem);
   unsigned char* stage = copy_smem + kBulkHeader;
@@ -255,10 +259,10 @@ extern "C" int kv_copy_blocks(void* k_cache, void* v_cache, int32_t num_layers,
   const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);
   auto k4 = copy_blocks_kernel<4>;
   auto k1 = copy_blocks_kernel<1>;
-  (grouped ? k4 : k1)<<<grid, kThreads, 0, stream>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks, block_size,
-      num_layers, (int32_t)(row_bytes / 16), src_blocks, dst_blocks, num_pairs, d_err);
-  return launch_status();
+  return launch_pdl(grouped ? k4 : k1, grid, kThreads, 0, stream, static_cast<uint4*>(k_cache),
+                    static_cast<uint4*>(v_cache), num_blocks, block_size, num_layers,
+                    (int32_t)(row_bytes / 16), src_blocks, dst_blocks, (int64_t)num_pairs,
+                    d_err);
 }
 
 extern "C" int kv_copy_blocks_bulk(void* k_cache, void* v_cache, int32_t num_layers,
@@ -277,8 +281,8 @@ extern "C" int kv_copy_blocks_bulk(void* k_cache, void* v_cache, int32_t num_lay
                            (int)kBulkSmem) != cudaSuccess)
     return KV_ECUDA;
   const int grid = sm_count() * kBulkCtasPerSm;
-  copy_blocks_bulk_kernel<<<grid, 32, kBulkSmem, stream>>>(
-      static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache), num_blocks,
-      num_layers, block_bytes, (int32_t)pieces, src_blocks, dst_blocks, num_pairs, d_err);
-  return launch_status();
+  return launch_pdl(copy_blocks_bulk_kernel, grid, 32, kBulkSmem, stream,
+                    static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache),
+                    num_blocks, num_layers, block_bytes, (int32_t)pieces, src_blocks, dst_blocks,
+                    (int64_t)num_pairs, d_err);
 }

@@ -32,6 +32,8 @@ template <bool kVec4>
 __global__ void __launch_bounds__(kThreads)
 expand_kernel(const int32_t* __restrict__ mgr, int32_t num_reqs, int32_t mgr_stride, int32_t k,
               int32_t* __restrict__ out, int32_t kernel_stride, int32_t* err_word) {
+  pdl_allow_next();
+  pdl_wait();
   uint32_t err = 0;
   const int32_t groups = (kernel_stride + 3) / 4;
   const int64_t total = (int64_t)num_reqs * groups;
@@ -82,11 +84,6 @@ extern "C" int kv_expand_kernel_blocks(const int32_t* mgr_table, int32_t num_req
   const int64_t ctas = (groups + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)sm_count() * (2048 / kThreads);
   const int grid = (int)(ctas < cap ? ctas : cap);
-  if (vec4)
-    expand_kernel<true><<<grid, kThreads, 0, stream>>>(mgr_table, num_reqs, mgr_stride, k,
-                                                       kernel_table, kernel_stride, d_err);
-  else
-    expand_kernel<false><<<grid, kThreads, 0, stream>>>(mgr_table, num_reqs, mgr_stride, k,
-                                                        kernel_table, kernel_stride, d_err);
-  return launch_status();
+  return launch_pdl(vec4 ? expand_kernel<true> : expand_kernel<false>, grid, kThreads, 0, stream,
+                    mgr_table, num_reqs, mgr_stride, k, kernel_table, kernel_stride, d_err);
 }

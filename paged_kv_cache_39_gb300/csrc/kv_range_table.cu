@@ -28,6 +28,8 @@ table_from_ranges_kernel(const int32_t* __restrict__ range_start,
                          const int32_t* __restrict__ num_ranges, int32_t rstride,
                          int32_t num_reqs, int32_t* __restrict__ table, int32_t tstride,
                          int32_t* err_word) {
+  pdl_allow_next();
+  pdl_wait();
   __shared__ int64_t s_cum[kThreads];   // first logical block of range i
   __shared__ int64_t s_end[kThreads];   // first logical block after range i
   __shared__ int32_t s_start[kThreads];
@@ -114,8 +116,6 @@ extern "C" int kv_table_from_ranges(const int32_t* range_start, const int32_t* r
   const int64_t units = (int64_t)num_reqs * chunks;
   const int64_t cap = (int64_t)sm_count() * (2048 / kThreads);
   const int grid = (int)(units < cap ? units : cap);
-  table_from_ranges_kernel<<<grid, kThreads, 0, stream>>>(range_start, range_len, num_ranges,
-                                                          range_stride, num_reqs, block_table,
-                                                          table_stride, d_err);
-  return launch_status();
+  return launch_pdl(table_from_ranges_kernel, grid, kThreads, 0, stream, range_start, range_len,
+                    num_ranges, range_stride, num_reqs, block_table, table_stride, d_err);
 }

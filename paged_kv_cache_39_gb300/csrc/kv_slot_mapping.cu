@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kThreads)
 slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t stride,
                           bool qsl_in_smem, CpArgs cp) {
   constexpr bool kCP = kMode == PagedMode::kCP;
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ int32_t s_qsl[];
   const int32_t base = blockIdx.x * (kThreads * kTokPerThread) + threadIdx.x;
   // positions do not depend on the request: start their loads first
@@ -233,6 +235,8 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
                           const int32_t* __restrict__ range_len,
                           const int32_t* __restrict__ num_ranges, int32_t rstride,
                           bool qsl_in_smem, bool vec4) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ int32_t s_qsl[];
   // positions staged per thread in shared memory: all loads are issued at
   // once, and the token loop below stays rolled (one copy of its search
@@ -430,13 +434,9 @@ int launch_paged(const int32_t* query_start_loc, const int64_t* positions,
   SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens,
              BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
   const bool st = staged && num_reqs > 0;
-  if (tpt == 1)
-    slot_mapping_paged_kernel<1, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                          table_stride, st, cp);
-  else
-    slot_mapping_paged_kernel<4, kMode><<<grid, kThreads, smem, stream>>>(a, block_table,
-                                                                          table_stride, st, cp);
-  return launch_status();
+  return launch_pdl(tpt == 1 ? slot_mapping_paged_kernel<1, kMode>
+                              : slot_mapping_paged_kernel<4, kMode>,
+                    grid, kThreads, smem, stream, a, block_table, table_stride, st, cp);
 }
 
 }  // namespace
@@ -510,14 +510,9 @@ extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64
              BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
   const bool st = staged && num_reqs > 0;
   const bool v4 = rows_vec4(range_start, range_len, range_stride);
-  if (tpt == 1)
-    slot_mapping_range_kernel<1><<<grid, kThreads, smem, stream>>>(
-        a, range_start, range_len, num_ranges, range_stride, st, v4);
-  else if (tpt == 4)
-    slot_mapping_range_kernel<4><<<grid, kThreads, smem, stream>>>(
-        a, range_start, range_len, num_ranges, range_stride, st, v4);
-  else
-    slot_mapping_range_kernel<8><<<grid, kThreads, smem, stream>>>(
-        a, range_start, range_len, num_ranges, range_stride, st, v4);
-  return launch_status();
+  auto kernel = tpt == 1   ? slot_mapping_range_kernel<1>
+                : tpt == 4 ? slot_mapping_range_kernel<4>
+                           : slot_mapping_range_kernel<8>;
+  return launch_pdl(kernel, grid, kThreads, smem, stream, a, range_start, range_len, num_ranges,
+                    range_stride, st, v4);
 }

@@ -160,6 +160,8 @@ __device__ __forceinline__ void store_unit(const RowArgs& w, const SlotArgs& a, 
 template <class Lookup>
 __global__ void __launch_bounds__(kThreads, 4)
 slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4) {
+  pdl_allow_next();
+  pdl_wait();
   extern __shared__ int32_t s_qsl[];
   const int lane = threadIdx.x & 31;
   const int32_t t = blockIdx.x * kWarps + (int32_t)(threadIdx.x >> 5);  // warp-uniform
@@ -280,8 +282,8 @@ int launch_slot_write(const int32_t* qsl, const int64_t* positions, const Lookup
              num_blocks, slot_mapping, d_err};
   RowArgs w{static_cast<const uint4*>(key), static_cast<const uint4*>(value),
             static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_layers, row_vecs};
-  slot_write_kernel<Lookup><<<grid, kThreads, smem, stream>>>(a, lk, w, staged, vec4);
-  return launch_status();
+  return launch_pdl(slot_write_kernel<Lookup>, grid, kThreads, smem, stream, a, lk, w, staged,
+                    vec4);
 }
 
 }  // namespace
