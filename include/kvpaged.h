@@ -27,6 +27,10 @@
  *   (for example a torch CUDA tensor).  The library allocates nothing, keeps
  *   no state between calls and never synchronises: each call validates its
  *   host-visible arguments, enqueues one kernel on `stream` and returns.
+ *   Kernels are launched with programmatic dependent launch: one may be
+ *   scheduled while the previous kernel on the stream is finishing, but it
+ *   waits for that kernel to complete before its first memory access, so the
+ *   results are those of plain stream order (also inside CUDA graphs).
  *   A pointer may be NULL only where the call reads nothing through it (for
  *   example `positions` when num_tokens == 0).
  * Layouts.  All arrays are dense, row-major, without padding between rows
