@@ -64,7 +64,7 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
   // phase 1: table index of every token of the thread (-1: PAD without lookup)
   int64_t idx[kTokPerThread], off[kTokPerThread];
-  ReqSpan last_r;
+  int last_r = -1;
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) {
     const int32_t t = base + k * kThreads;
