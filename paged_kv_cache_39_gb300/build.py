@@ -36,16 +36,23 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(verbose: bool = False, ptxas_info: bool = False, host_flags=(), out: str = None,
+          build_dir: str = None) -> str:
+    """Compile every translation unit and link the library.  `host_flags`
+    go to the host compiler and linker, one flag each (nvcc splits a flag at
+    commas), e.g. sanitizers for a test build; `out` / `build_dir` place such
+    a variant away from the product build."""
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    bdir = build_dir or BUILD_DIR
+    os.makedirs(bdir, exist_ok=True)
+    host = [x for f in host_flags for x in ("-Xcompiler", f)]
     common = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]
+              "-Xcompiler", "-Wall", *host, "-I", INCLUDE, "-I", CSRC]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -58,9 +65,9 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         for obj, log in results:
             if log.strip():
                 print(f"== {os.path.basename(obj)}\n{log}")
-    out = library_path()
+    out = out or library_path()
     tmp = out + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
+    cmd = [nvcc, *ARCH, "-shared", *host, "-o", tmp, *[o for o, _ in results], "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -14,6 +14,14 @@ HEADER = os.path.join(ROOT, "include", "kvpaged.h")
 def lib():
     from paged_kv_cache_39_gb300 import _lib
     from paged_kv_cache_39_gb300 import build as kbuild
+    variant = os.environ.get("KV_TEST_LIB")  # a sanitizer build of the same sources
+    if variant:
+        import ctypes
+        l = ctypes.CDLL(variant)
+        for name, (args, res) in _lib.SIGNATURES.items():
+            getattr(l, name).argtypes = args
+            getattr(l, name).restype = res
+        return l
     if not os.path.exists(_lib.LIB_PATH):
         kbuild.build()
     return _lib.load()
