@@ -28,6 +28,12 @@
  *   bf16 values are copied as raw 16-bit patterns: every output is an integer
  *   or copied bits, so results are exact.
  *
+ * Parity status: every function is pinned by the tests to the pages' worked
+ * examples, closed forms, brute force or invariants, except the
+ * context-parallel filter (orc_slot_mapping_paged_cp): PARITY UNPINNED beyond
+ * world size 1, its formula being cut off on the pages (a reading; pinned only
+ * at world size 1 and by partition/distinctness properties).
+ *
  * Error word bits (OR-ed into *err; identical meaning in the CUDA library):
  *   1 BAD_BLOCK, 2 BAD_SLOT, 4 BAD_POSITION, 8 BAD_RANGE, 16 NULL_WRITE,
  *   32 BAD_QSL, 64 OUT_OF_SPACE.
