@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_kv_cache_39_gb300 as kv
 from paged_kv_cache_39_gb300 import workloads as wl
-from gpu_helpers import bits, dev, err_word
+from gpu_helpers import bits, cuda, dev, err_word
 
 pytestmark = pytest.mark.gpu
 
@@ -161,3 +161,85 @@ def test_bounded_wait_times_out_and_context_survives():
     e2 = err_word()
     s = kv.kv_slot_mapping_paged(q, p, t, 16, 8, max_num_tokens=5, err=e2)
     assert s.cpu().tolist() == [48, 49, 65, -1, -1] and int(e2.item()) == 0
+
+
+def test_every_prepared_call_matches_its_direct_call():
+    """prepare=True on each wrapper: the relaunched call reads the inputs as
+    they are at launch time (contents changed after preparing) and gives the
+    direct call's outputs and error word."""
+    rng = np.random.default_rng(8100)
+    T, B, H, D, R, S = 16, 64, 2, 64, 6, 4
+    runs = rng.permutation(np.arange(1, B)).astype(np.int32)[:R * S].reshape(R, S)
+    table = runs.copy()
+    rs, rl, nr = runs.copy(), np.ones((R, S), np.int32), np.full(R, S, np.int32)
+    lens = rng.integers(1, 5, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+
+    def positions():
+        return np.concatenate([rng.choice(S * T, size=n, replace=False)
+                               for n in lens]).astype(np.int64)
+
+    d = {"q": cuda(q), "pos": cuda(positions()), "table": cuda(table), "rs": cuda(rs),
+         "rl": cuda(rl), "nr": cuda(nr), "g0": cuda(np.zeros(R, np.int32)),
+         "g1": cuda(np.full(R, S * T, np.int32)), "mgr": cuda(table[:, :2]),
+         "src": cuda(np.array([table[0, 0]], np.int32)),
+         "dst": cuda(np.array([table[1, 0]], np.int32))}
+    key = wl.bf16_normal((1, N, H, D), 8101, dev())
+    caches = {n: wl.bf16_normal((1, B, T, H, D), 8102, dev()) for n in ("p", "d")}
+    outs = {n: torch.zeros((R * S * T, H, D), dtype=torch.bfloat16, device=dev())
+            for n in ("p", "d")}
+    calls = {
+        "paged": lambda o, **k: kv.kv_slot_mapping_paged(d["q"], d["pos"], d["table"], T, B,
+                                                         slot_mapping=o, **k),
+        "range": lambda o, **k: kv.kv_slot_mapping_range(d["q"], d["pos"], d["rs"], d["rl"],
+                                                         d["nr"], T, B, slot_mapping=o, **k),
+        "cp": lambda o, **k: kv.kv_slot_mapping_paged_cp(d["q"], d["pos"], d["table"], T, B, 2,
+                                                         1, 1, slot_mapping=o, **k),
+        "expand": lambda o, **k: kv.kv_expand_kernel_blocks(d["mgr"], 2 * T, T,
+                                                            kernel_table=o, **k),
+        "table": lambda o, **k: kv.kv_table_from_ranges(d["rs"], d["rl"], d["nr"],
+                                                        block_table=o, **k),
+    }
+    shapes = {"paged": (N,), "range": (N,), "cp": (N,), "expand": (R, 4), "table": (R, S)}
+    dtypes = {"paged": torch.int64, "range": torch.int64, "cp": torch.int64,
+              "expand": torch.int32, "table": torch.int32}
+    prepared = {}
+    for name, fn in calls.items():
+        o = torch.empty(shapes[name], dtype=dtypes[name], device=dev())
+        e = err_word()
+        prepared[name] = (fn(o, err=e, prepare=True), o, e)
+    kc, vc = caches["p"], caches["p"].clone()
+    sp = torch.empty(N, dtype=torch.int64, device=dev())
+    ep = err_word()
+    p_write = kv.kv_slot_mapping_paged_write(d["q"], d["pos"], d["table"], T, B, key, key, kc, vc,
+                                             slot_mapping=sp, err=ep, prepare=True)
+    p_gather = kv.kv_cache_gather_range(kc, vc, d["rs"], d["rl"], d["nr"], d["g0"], d["g1"],
+                                        k_out=outs["p"], v_out=outs["p"].clone(),
+                                        out_rows=R * S * T, err=ep, prepare=True)
+    p_copy = kv.kv_copy_blocks(kc, vc, d["src"], d["dst"], err=ep, bulk=True, prepare=True)
+    # new contents after preparing: the prepared calls must see them
+    d["pos"].copy_(cuda(positions()))
+    for name, (pc, o, e) in prepared.items():
+        pc()
+        o2 = torch.empty_like(o)
+        e2 = err_word()
+        calls[name](o2, err=e2)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o2) and int(e.item()) == int(e2.item()), name
+    p_write()
+    p_copy()
+    p_gather()
+    kd, vd = caches["d"], caches["d"].clone()
+    sd = torch.empty(N, dtype=torch.int64, device=dev())
+    ed = err_word()
+    kv.kv_slot_mapping_paged_write(d["q"], d["pos"], d["table"], T, B, key, key, kd, vd,
+                                   slot_mapping=sd, err=ed)
+    kv.kv_copy_blocks(kd, vd, d["src"], d["dst"], err=ed, bulk=True)
+    ko = outs["d"]
+    kv.kv_cache_gather_range(kd, vd, d["rs"], d["rl"], d["nr"], d["g0"], d["g1"], k_out=ko,
+                             v_out=ko.clone(), out_rows=R * S * T, err=ed)
+    torch.cuda.synchronize()
+    assert torch.equal(sp, sd) and int(ep.item()) == int(ed.item()) == 0
+    assert torch.equal(kc.view(torch.int16), kd.view(torch.int16))
+    assert torch.equal(outs["p"].view(torch.int16), ko.view(torch.int16))
