@@ -632,23 +632,33 @@ def host_decode_state(wl, seed=1):
     return w, lay, kc_h, vc_h, key_h, val_h
 
 
-def cpu_baseline(seconds):
+def cpu_baseline(seconds, rounds=5):
+    """The oracle's decode step on one host core, timed in the pages' host-bench
+    manner: `rounds` rounds, one warm-up call per round, then whole steps for
+    seconds / rounds; value = mean of the per-round rates, with their stddev."""
     import oracle
     from paged_kv_cache_39_gb300 import workloads as wl
     w, lay, kc_h, vc_h, key_h, val_h = host_decode_state(wl)
-    oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 8)  # warm
-    t0 = time.perf_counter()
-    steps, toks = 0, 0
-    while True:
-        toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, w.num_reqs)
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": round(toks / el, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} whole decode step(s) of the oracle (both slot maps, the write and "
-                      f"the {int((w.gather_end - w.gather_start).sum())}-row context gather), "
-                      f"single-threaded, {el:.1f} s",
+    rates, steps_total, el_total = [], 0, 0.0
+    for _ in range(rounds):
+        oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 8)  # warm-up call
+        t0 = time.perf_counter()
+        steps, toks = 0, 0
+        while True:
+            toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, w.num_reqs)
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds / rounds:
+                break
+        rates.append(toks / el)
+        steps_total += steps
+        el_total += el
+    return {"value": round(statistics.mean(rates), 1),
+            "stddev": round(statistics.stdev(rates), 1) if rounds > 1 else 0.0,
+            "rounds": rounds, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps_total} whole decode step(s) of the oracle (both slot maps, the "
+                      f"write and the {int((w.gather_end - w.gather_start).sum())}-row context "
+                      f"gather) in {rounds} rounds, single-threaded, {el_total:.1f} s",
             "host_cores": os.cpu_count()}
 
 
