@@ -123,3 +123,29 @@ def random_slot_case(rng):
     table[rng.random(table.shape) < 0.2] = 0
     pos = rng.integers(-2, max(stride, 1) * T + 20, size=N).astype(np.int64)
     return T, R, q.astype(np.int32), N, n_max, stride, B, table, pos
+
+
+def check_write_vs_before(key, val, kc, vc, kc0, vc0, slots_host, L, N, B, T, E, rng):
+    """check_write for caches of random contents.  kc0/vc0 are copies taken
+    before the write (consumed here): the oracle's destination rows are set in
+    them to their tokens' rows, after which the written caches must equal
+    them whole, so every row the write must not touch is checked too."""
+    dest, exp_e = oracle.write_rows(slots_host, N, L, B, T)
+    flat_dest = dest.reshape(-1)
+    valid = np.nonzero(flat_dest >= 0)[0]
+    src_k, src_v = rows_view(key, E), rows_view(val, E)
+    kr0, vr0 = rows_view(kc0, E), rows_view(vc0, E)
+    for s in range(0, len(valid), 1 << 16):
+        sel = torch.from_numpy(valid[s:s + (1 << 16)]).to(dev())
+        drow = torch.from_numpy(flat_dest[valid[s:s + (1 << 16)]]).to(dev())
+        kr0[drow] = src_k.index_select(0, sel)
+        vr0[drow] = src_v.index_select(0, sel)
+    assert torch.equal(rows_view(kc, E), kr0) and torch.equal(rows_view(vc, E), vr0)
+    # sampled host check through the oracle's per-row arithmetic
+    kr = rows_view(kc, E)
+    pick = rng.choice(len(valid), size=min(256, len(valid)), replace=False)
+    for i in valid[pick]:
+        l, t = divmod(int(i), N)
+        got = kr[int(flat_dest[i])].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, src_k[l * N + t].cpu().numpy().view(np.uint16))
+    return exp_e

@@ -15,8 +15,9 @@ import torch
 import oracle
 import paged_kv_cache_39_gb300 as kv
 from paged_kv_cache_39_gb300 import workloads as wl
-from gpu_helpers import (FILL, SAMPLE, check_write, cuda, dev, device_rows_equal, err_word,
-                         filled_cache, free_bytes, rows_view, sample_host_check)
+from gpu_helpers import (FILL, SAMPLE, check_write, check_write_vs_before, cuda, dev,
+                         device_rows_equal, err_word, filled_cache, free_bytes, rows_view,
+                         sample_host_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,38 +56,49 @@ def slot_maps_match(w, lay, check_range=True):
 
 
 def test_decode_full():
+    """The decode batch: slot maps, the write into caches of random contents
+    (every other row unchanged), then the gather of every request's whole
+    context (597k rows, all distinct), checked row by row against the
+    oracle's source rows."""
     w = wl.decode()
     lay = w.layouts["G"]
     T, B, H, D, E = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim, w.row_elems
     sp, exp = slot_maps_match(w, lay)
     key = wl.bf16_normal((1, w.num_tokens, H, D), 101, dev())
     val = wl.bf16_normal((1, w.num_tokens, H, D), 102, dev())
-    kc, vc = filled_cache((1, B, T, H, D)), filled_cache((1, B, T, H, D))
+    kc = wl.bf16_normal((1, B, T, H, D), 103, dev())
+    vc = wl.bf16_normal((1, B, T, H, D), 104, dev())
+    kc0, vc0 = kc.clone(), vc.clone()
     e = err_word()
     kv.kv_cache_write(key, val, kc, vc, sp, err=e)
-    exp_e = check_write(key, val, kc, vc, exp, 1, w.num_tokens, B, T, E,
-                        np.random.default_rng(1))
+    exp_e = check_write_vs_before(key, val, kc, vc, kc0, vc0, exp, 1, w.num_tokens, B, T, E,
+                                  np.random.default_rng(1))
     assert int(e.item()) == exp_e == 0
+    del kc0, vc0
     # the decode batch's contexts read back through the table: the new token
     # is the last row of each request's span
     rows = int(w.gather_end.sum())
-    e = err_word()
-    k_out, v_out = kv.kv_cache_gather(kc, vc, cuda(lay.table), cuda(w.gather_start),
-                                      cuda(w.gather_end), out_rows=rows, err=e)
     src, exp_ge = oracle.gather_rows(0, B, T, lay.table, w.gather_start, w.gather_end, rows)
-    assert int(e.item()) == exp_ge == 0
-    assert device_rows_equal(k_out, kc, src, E) and device_rows_equal(v_out, vc, src, E)
-    last = np.cumsum(w.gather_end.astype(np.int64)) - 1
-    assert torch.equal(rows_view(k_out, E)[torch.from_numpy(last).to(dev())], rows_view(key[0], E))
+    assert (src >= 0).all() and len(np.unique(src)) == rows
+    for bulk in (False, True):
+        e = err_word()
+        k_out, v_out = kv.kv_cache_gather(kc, vc, cuda(lay.table), cuda(w.gather_start),
+                                          cuda(w.gather_end), out_rows=rows, err=e, bulk=bulk)
+        assert int(e.item()) == exp_ge == 0
+        assert device_rows_equal(k_out, kc, src, E) and device_rows_equal(v_out, vc, src, E)
+        last = np.cumsum(w.gather_end.astype(np.int64)) - 1
+        sel = torch.from_numpy(last).to(dev())
+        assert torch.equal(rows_view(k_out, E)[sel], rows_view(key[0], E))
+        assert torch.equal(rows_view(v_out, E)[sel], rows_view(val[0], E))
+        sample = np.sort(np.random.default_rng(11).choice(rows, size=SAMPLE, replace=False))
+        kflat = rows_view(kc, E)
+        sample_host_check(k_out, lambda n: kflat[n].cpu().numpy().view(np.uint16), src, E,
+                          sample)
+        del k_out, v_out
 
 
 def test_mixed_full():
-    need = 2 * 32 * 49152 * 16 * 2048 + (8 << 30)
-    if free_bytes() >= need:
-        w = wl.mixed()
-    else:  # reduced pool, recorded in the test output
-        print("mixed: reduced to 32768 blocks / decode ctx U{512..2048} for free memory")
-        w = wl.mixed(num_blocks=32768, decode_ctx_max=2048)
+    w = mixed_workload()
     lay = w.layouts["G"]
     T, B, L, H, D, E = (w.block_size, w.num_blocks, w.num_layers, w.num_kv_heads, w.head_dim,
                         w.row_elems)
@@ -100,6 +112,73 @@ def test_mixed_full():
     assert int(e.item()) == exp_e == 0
     # null block 0 of every layer is untouched
     assert (kc.view(torch.int16)[:, 0] == FILL).all() and (vc.view(torch.int16)[:, 0] == FILL).all()
+
+
+def mixed_workload():
+    if free_bytes() >= 2 * 32 * 49152 * 16 * 2048 + (12 << 30):
+        return wl.mixed()
+    print("mixed: reduced to 32768 blocks / decode ctx U{512..2048} for free memory")
+    return wl.mixed(num_blocks=32768, decode_ctx_max=2048)
+
+
+def test_mixed_gather_layers():
+    """Gathers from the 32-layer mixed caches (51.5 GB each, random contents)
+    at layers 0, 17 and 31, where layer * num_blocks * block_size * row_bytes
+    puts byte offsets far past 2^32: the table gather, its bulk-copy form and
+    the range-addressed gather, every row against the oracle's source rows.
+    The batch is written first, so the gathered spans also hold the new
+    tokens' rows (gather after write returns what was written)."""
+    w = mixed_workload()
+    lay = w.layouts["G"]
+    T, B, L, H, D, E = (w.block_size, w.num_blocks, w.num_layers, w.num_kv_heads, w.head_dim,
+                        w.row_elems)
+    N = w.num_tokens
+    kc = wl.bf16_normal((L, B, T, H, D), 501, dev())
+    vc = wl.bf16_normal((L, B, T, H, D), 502, dev())
+    key = wl.bf16_normal((L, N, H, D), 503, dev())
+    val = wl.bf16_normal((L, N, H, D), 504, dev())
+    exp_s, _ = oracle.slot_mapping_paged(w.qsl, w.positions, lay.table, N, N, T, B)
+    e = err_word()
+    sp = kv.kv_slot_mapping_paged(cuda(w.qsl), cuda(w.positions), cuda(lay.table), T, B, err=e)
+    kv.kv_cache_write(key, val, kc, vc, sp, err=e)
+    assert int(e.item()) == 0
+    dest, _ = oracle.write_rows(exp_s, N, L, B, T)  # absolute cache row of (layer, token)
+    rows = int((w.gather_end.astype(np.int64) - w.gather_start).sum())
+    table, g0, g1 = cuda(lay.table), cuda(w.gather_start), cuda(w.gather_end)
+    rs, rl, nr = cuda(lay.range_start), cuda(lay.range_len), cuda(lay.num_ranges)
+    kflat = rows_view(kc, E)
+    rng = np.random.default_rng(12)
+    for layer in (0, 17, 31):
+        src, exp_ge = oracle.gather_rows(layer, B, T, lay.table, w.gather_start, w.gather_end,
+                                         rows)
+        assert exp_ge == 0 and (src >= 0).all()
+        assert src.min() >= layer * B * T and src.max() < (layer + 1) * B * T
+        # output rows whose source is a row the write just filled, and its token
+        order = np.argsort(dest[layer])
+        at = np.searchsorted(dest[layer][order], src)
+        hit = (at < N) & (dest[layer][order][np.minimum(at, N - 1)] == src)
+        assert int(hit.sum()) == N  # every new token is read back exactly once
+        o_new = torch.from_numpy(np.nonzero(hit)[0]).to(dev())
+        t_new = torch.from_numpy(order[at[hit]]).to(dev())
+        outs = {}
+        for form in ("table", "bulk", "range"):
+            e = err_word()
+            if form == "range":
+                ko, vo = kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, layer=layer,
+                                                  out_rows=rows, err=e)
+            else:
+                ko, vo = kv.kv_cache_gather(kc, vc, table, g0, g1, layer=layer, out_rows=rows,
+                                            err=e, bulk=form == "bulk")
+            assert int(e.item()) == 0, (layer, form)
+            assert device_rows_equal(ko, kc, src, E) and device_rows_equal(vo, vc, src, E), \
+                (layer, form)
+            assert torch.equal(rows_view(ko, E)[o_new], rows_view(key[layer], E)[t_new])
+            assert torch.equal(rows_view(vo, E)[o_new], rows_view(val[layer], E)[t_new])
+            outs[form] = (ko, vo)
+        sample = np.sort(rng.choice(rows, size=SAMPLE, replace=False))
+        sample_host_check(outs["table"][0], lambda n: kflat[n].cpu().numpy().view(np.uint16),
+                          src, E, sample)
+        del outs
 
 
 @pytest.mark.parametrize("layout", ["P", "G"])

@@ -79,7 +79,8 @@ def test_table_from_ranges_rebuilds_workload_tables(name, layout):
 
 @pytest.mark.parametrize("seed,R,S,H,D", [(0, 1, 4, 8, 128), (1, 6, 6, 8, 64), (2, 300, 3, 1, 8),
                                           (3, 4096, 2, 1, 16), (4, 17, 40, 16, 128),
-                                          (5, 9, 256, 2, 72)])
+                                          (5, 9, 256, 2, 72), (6, 4093, 2, 1, 8),
+                                          (7, 4095, 1, 1, 8)])
 def test_gather_range_random_parity(seed, R, S, H, D):
     rng = np.random.default_rng(9100 + seed)
     T, B, L = 8, 60, 2
