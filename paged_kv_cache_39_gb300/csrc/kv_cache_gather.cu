@@ -26,6 +26,9 @@ constexpr int kThreads = 256;
 constexpr int kVecPerLane = 4;
 constexpr int kChunkVecs = 32 * kVecPerLane;
 constexpr int kRowsPerWarp = 4;
+// static shared memory of the two vector kernels (the per-warp scan totals);
+// it counts against the 48 KiB a launch gets without opting in
+constexpr size_t kGatherStaticSmem = sizeof(int64_t) * (kThreads / 32);
 
 struct GatherArgs {
   const uint4* k_cache;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) cache_gather_kernel(GatherArgs a) {
   extern __shared__ int64_t smem[];
   int64_t* s_off = smem;                                                 // [num_reqs + 1]
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + a.num_reqs + 1);  // [num_reqs]
-  __shared__ int64_t s_warp_sum[kThreads / 32];
+  __shared__ int64_t s_warp_sum[kGatherStaticSmem / sizeof(int64_t)];
   uint32_t err = 0;
   const int64_t total = packed_offsets(a, s_off, s_start, s_warp_sum, err);
   const int64_t rows = total < a.out_rows ? total : a.out_rows;
@@ -243,7 +246,7 @@ cache_gather_range_kernel(GatherArgs a, const int32_t* __restrict__ range_start,
   extern __shared__ int64_t smem[];
   int64_t* s_off = smem;
   int32_t* s_start = reinterpret_cast<int32_t*>(smem + a.num_reqs + 1);
-  __shared__ int64_t s_warp_sum[kThreads / 32];
+  __shared__ int64_t s_warp_sum[kGatherStaticSmem / sizeof(int64_t)];
   uint32_t err = 0;
   // descriptor-row validation, every request, grid-wide
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < a.num_reqs;
@@ -493,7 +496,7 @@ static int launch_gather(Kernel kernel, const GatherArgs& a, Extra... extra) {
   const int64_t ctas_needed = (a.out_rows + rows_per_cta - 1) / rows_per_cta;
   const int64_t cap = (int64_t)sm_count() * (2048 / kThreads);
   const int grid = (int)(ctas_needed < 1 ? 1 : (ctas_needed < cap ? ctas_needed : cap));
-  if (smem > 48 * 1024 &&
+  if (smem + kGatherStaticSmem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return KV_ECUDA;
