@@ -82,8 +82,24 @@ enum kv_error_bits {
     KV_ERR_BAD_QSL = 32,      /* query_start_loc decreasing, negative, or past num_tokens */
     KV_ERR_OUT_OF_SPACE = 64, /* gather rows exceed out_rows, or ranges exceed a table row */
     KV_ERR_TIMEOUT = 128      /* an asynchronous bulk copy did not complete within the bounded
-                                 wait; the kernel stopped early and its output is incomplete */
+                                 wait (see "Bounded waits" below) */
 };
+
+/*
+ * Bounded waits.  Only the two bulk-copy calls (kv_cache_gather_bulk,
+ * kv_copy_blocks_bulk) wait on the copy engine, and every such wait gives up
+ * after 1 s of GPU time (the global nanosecond timer) or 2^22 tries,
+ * whichever comes first; a CTA that gave up waits once more, with the same
+ * bound, for each of its own loads still in flight, then ends.  A healthy
+ * copy completes in microseconds, so a timeout means the GPU is in trouble.
+ * After a call has set KV_ERR_TIMEOUT:
+ *   - its outputs are undefined: rows may be missing, partly written, or
+ *     written after the kernel ended (a load still in flight when its CTA
+ *     gave up), so do not use them;
+ *   - treat later results on the same stream as suspect until the stream has
+ *     been synchronised and checked for CUDA errors.
+ * No wait in this library is unbounded.
+ */
 
 #define KV_PAD_SLOT_ID (-1)
 #define KV_NULL_BLOCK_ID 0
@@ -309,9 +325,9 @@ int kv_cache_gather(const void* k_cache, const void* v_cache, int32_t layer, int
  * at most 32 KiB per copy) issued by a single thread per CTA, two one-warp
  * CTAs per SM: the whole-block gather with TMA bulk copies.  It reaches the
  * same bandwidth as kv_cache_gather while occupying 64 threads per SM, which
- * leaves the SMs to concurrent kernels.  Every wait for a copy is bounded: if
- * one ever ran out, KV_ERR_TIMEOUT is set and that CTA's remaining rows are
- * left unwritten.
+ * leaves the SMs to concurrent kernels.  Every wait for a copy is bounded
+ * (see "Bounded waits"): if one ever ran out, KV_ERR_TIMEOUT is set and the
+ * call's outputs are undefined.
  * Errors: as kv_cache_gather; KV_EUNSUPPORTED for a row of more than 32 KiB
  * (num_kv_heads * head_dim * 2 > 32768) or num_reqs > 2048.
  */
@@ -432,8 +448,9 @@ int kv_copy_blocks(void* k_cache, void* v_cache, int32_t num_layers, int64_t num
  * The same arguments, results, error bits and rules as kv_copy_blocks.  Each
  * K or V block of a (pair, layer) -- or each 32 KiB piece of a larger block --
  * goes global -> shared -> global with cp.async.bulk from one thread per
- * one-warp CTA, two CTAs per SM.  Every wait on the copy engine is bounded:
- * one that runs out sets KV_ERR_TIMEOUT and the kernel ends normally.
+ * one-warp CTA, two CTAs per SM.  Every wait on the copy engine is bounded
+ * (see "Bounded waits"): one that runs out sets KV_ERR_TIMEOUT, the kernel
+ * ends normally, and the destination blocks are undefined.
  * Errors: as kv_copy_blocks; KV_ECUDA if the shared-memory size cannot be set.
  */
 int kv_copy_blocks_bulk(void* k_cache, void* v_cache, int32_t num_layers, int64_t num_blocks,

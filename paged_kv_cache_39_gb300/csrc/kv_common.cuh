@@ -157,9 +157,20 @@ __device__ __forceinline__ T warp_inclusive_scan(T v) {
 // Bulk asynchronous copies (cp.async.bulk) and shared-memory mbarriers.
 // Global->shared copies complete a transaction count on an mbarrier;
 // shared->global copies are tracked in bulk groups per issuing thread.
-// Every wait on an mbarrier in this library is bounded (kSpinLimit tries).
+// Every wait on an mbarrier in this library is bounded twice: by kSpinLimit
+// tries and by kWaitLimitNs of wall time on the GPU's global nanosecond timer,
+// whichever runs out first.  A try may suspend the thread for a
+// hardware-defined interval, so the try count alone would not bound the time;
+// the timer does (a healthy copy completes in microseconds).
 
 constexpr long kSpinLimit = 1L << 22;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -186,11 +197,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase of the given parity; false when the limit ran out.
+// Bounded wait for the phase of the given parity; false when either limit ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  long limit = kSpinLimit) {
-  for (long i = 0; i < limit; ++i)
+                                                  long limit = kSpinLimit,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  const uint64_t t0 = global_ns();
+  for (long i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
   return false;
 }
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,

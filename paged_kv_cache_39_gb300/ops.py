@@ -301,7 +301,9 @@ def _gather_outputs(k_cache, gather_start, gather_end, k_out, v_out, out_rows, H
     _need(gather_end, "gather_end", torch.int32, dev)
     if k_out is None:
         if out_rows is None:
-            out_rows = int((gather_end.long() - gather_start.long()).clamp_min(0).sum().item())
+            # the total span length lives on the device: reading it back here
+            # would synchronise the stream inside an asynchronous call
+            raise ValueError("give out_rows (or k_out/v_out) for the gather")
         k_out = torch.empty((out_rows, H, D), dtype=torch.bfloat16, device=k_cache.device)
         v_out = torch.empty((out_rows, H, D), dtype=torch.bfloat16, device=k_cache.device)
     _need(k_out, "k_out", torch.bfloat16, dev)
@@ -321,9 +323,10 @@ def kv_cache_gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: t
                     prepare: bool = False):
     """Gather positions [start_r, end_r) of every request into packed [rows, H, D] buffers.
 
-    ``out_rows`` (or the given outputs' row count) must be at least the total
-    span length; when it is None and no outputs are given, the total is read
-    back from the device spans (a synchronising convenience for tests).
+    ``out_rows`` (or, when it is None, the given outputs' row count) must be
+    at least the total span length.  Without outputs ``out_rows`` is required:
+    the spans live on the device, and the call never reads them back (it does
+    not synchronise and can be captured in a CUDA graph).
     ``bulk=True`` calls kv_cache_gather_bulk (bulk-copy engine) instead.
     Returns (k_out, v_out).
     """
