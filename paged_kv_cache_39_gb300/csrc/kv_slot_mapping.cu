@@ -389,6 +389,247 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   report(a.err, err);
 }
 
+// ---------------------------------------------------------------------------
+// Range variant for large prefill batches and long contexts (4 or 8 tokens
+// per thread, requests long enough to fill a tile).  A CTA whose token tile
+// belongs to at most kStageReqs requests stages those requests' descriptors
+// in shared memory once: one load per descriptor for the whole CTA, a warp
+// per request turns the lengths into range ends (logical block ranges
+// [end_{i-1}, end_i)), and a barrier publishes them.  Each token then
+// resolves its block from shared memory: a binary search for the first end
+// past its logical block, skipped while the token stays inside the range the
+// thread resolved last -- the descriptor once per position block, arithmetic
+// per position.  Other tiles let each lane walk its own request's ranges.
+// The grid-wide sweep over every descriptor row sets BAD_RANGE as in the
+// kernel above.
+
+constexpr int kStageReqs = 8;  // requests a CTA stages (one warp each for the scan)
+static_assert(kStageReqs == kThreads / 32, "one warp scans each staged request");
+
+// Logical block lb of request r by a walk of its descriptor row in global
+// memory (pre_*: its first kLanePrefetch descriptors, nr: its count).
+// Sets win on success.
+__device__ __forceinline__ bool range_walk(const int32_t* __restrict__ rs,
+                                           const int32_t* __restrict__ rl, int nr,
+                                           const int32_t (&pre_s)[kLanePrefetch],
+                                           const int32_t (&pre_l)[kLanePrefetch], int r,
+                                           int64_t lb, RangeWindow& win) {
+  int64_t cum = 0;
+#pragma unroll
+  for (int i = 0; i < kLanePrefetch; ++i) {
+    if (i < nr) {
+      const int64_t len = max(pre_l[i], 0);
+      if (lb < cum + len) {
+        win = RangeWindow{r, cum, cum + len, pre_s[i]};
+        return true;
+      }
+      cum += len;
+    }
+  }
+  for (int i = kLanePrefetch; i < nr; ++i) {
+    const int64_t len = max(rl[i], 0);
+    if (lb < cum + len) {
+      win = RangeWindow{r, cum, cum + len, rs[i]};
+      return true;
+    }
+    cum += len;
+  }
+  return false;
+}
+
+// Staged row j (counts in s_cnt, range ends in s_end, starts in s_beg):
+// the range holding logical block lb, or false when no range does.
+__device__ __forceinline__ bool staged_find(const int64_t* s_end, const int32_t* s_beg,
+                                            const int32_t* s_cnt, int32_t rstride, int j,
+                                            int r, int64_t lb, RangeWindow& win) {
+  const int n = s_cnt[j];
+  const int64_t* e = s_end + (size_t)j * rstride;
+  if (n <= 0 || lb >= e[n - 1]) return false;
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {  // first range whose end passes lb
+    const int mid = (lo + hi) >> 1;
+    if (e[mid] > lb) hi = mid; else lo = mid + 1;
+  }
+  win = RangeWindow{r, lo > 0 ? e[lo - 1] : 0, e[lo], s_beg[(size_t)j * rstride + lo]};
+  return true;
+}
+
+// At most 64 registers: four CTAs per SM keep the grid within one wave
+// (512 CTAs for 1M positions at 8 tokens per thread); 80 registers left
+// three per SM and a second wave.
+template <int kTokPerThread>
+__global__ void __launch_bounds__(kThreads, 4)
+slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
+                                 const int32_t* __restrict__ range_len,
+                                 const int32_t* __restrict__ num_ranges, int32_t rstride,
+                                 bool qsl_in_smem, bool vec4) {
+  pdl_allow_next();
+  pdl_wait();
+  // dynamic shared memory: the staged range ends (int64) and starts
+  // (int32), kStageReqs rows of rstride each; then query_start_loc
+  extern __shared__ int64_t s_dyn[];
+  const size_t staged_entries = (size_t)kStageReqs * rstride;
+  int64_t* s_end = s_dyn;
+  int32_t* s_beg = reinterpret_cast<int32_t*>(s_end + staged_entries);
+  int32_t* s_qsl = s_beg + staged_entries;
+  // positions staged per thread in shared memory: the token loops stay
+  // rolled (one copy of their search paths keeps the instruction footprint
+  // small) and no register holds a position while it is in flight; only the
+  // thread itself reads its entries back
+  __shared__ int64_t s_pos[kTokPerThread][kThreads];
+  __shared__ int32_t s_cnt[kStageReqs];  // staged counts, -1: malformed row
+  constexpr int32_t kTile = kThreads * kTokPerThread;
+  const int32_t t_lo = blockIdx.x * kTile;
+  const int32_t base = t_lo + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  // the positions go straight to shared memory by asynchronous copies, in
+  // flight together with the qsl and descriptor staging loads below
+#pragma unroll
+  for (int k = 0; k < kTokPerThread; ++k) {
+    const int32_t t = base + k * kThreads;
+    if (t < a.num_tokens) cp_async8(&s_pos[k][threadIdx.x], a.positions + t);
+    else s_pos[k][threadIdx.x] = 0;
+  }
+  uint32_t err = 0;
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+
+  // descriptor-row validation, every request, grid-wide: the thread's first
+  // row is requested now and checked after the token loop, so the check costs
+  // no round trip on the loop's critical path
+  const int sweep0 = blockIdx.x * blockDim.x + threadIdx.x;
+  RangeRowCheck first_row;
+  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, sweep0, rstride, vec4);
+
+  // Requests of this tile: [st_lo, st_lo + st_n) when at most kStageReqs
+  // (every thread computes the same, CTA-uniform values).
+  const int32_t t_hi = min(t_lo + kTile, a.num_tokens);
+  int st_lo = 0, st_n = 0;
+  if (t_lo < t_hi && a.num_reqs > 0) {
+    const int r0 = max(find_span(q, a.num_reqs, t_lo), 0);
+    const int r1 = find_span(q, a.num_reqs, t_hi - 1);
+    if (r1 >= r0 && r1 - r0 < kStageReqs) {
+      st_lo = r0;
+      st_n = r1 - r0 + 1;
+    }
+  }
+  if (st_n > 0) {
+    // thread i loads descriptor i of every staged row, all loads in flight
+    // together, straight into shared memory (lengths as raw int64)
+    const int i = threadIdx.x;
+    if (i < st_n) s_cnt[i] = num_ranges[st_lo + i];
+    if (i < rstride) {
+#pragma unroll 2
+      for (int j = 0; j < kStageReqs; ++j) {
+        if (j < st_n) {
+          const int64_t row = (int64_t)(st_lo + j) * rstride;
+          s_beg[(size_t)j * rstride + i] = range_start[row + i];
+          s_end[(size_t)j * rstride + i] = range_len[row + i];
+        }
+      }
+    }
+    __syncthreads();
+    // warp j scans row j: its count is checked (-1: malformed, all PAD),
+    // lengths <= 0 count as empty, lane l sums a contiguous share of the
+    // row's first `count` entries, a warp scan of the shares, then the
+    // running sums (the range ends) are written back in place
+    if (wid < st_n) {
+      const int raw = s_cnt[wid];
+      const int n = (raw >= 0 && raw <= rstride) ? raw : -1;
+      __syncwarp();
+      if (lane == 0) s_cnt[wid] = n;
+      int64_t* e = s_end + (size_t)wid * rstride;
+      const int per = (max(n, 0) + 31) / 32;
+      const int i0 = lane * per, i1 = min(max(n, 0), i0 + per);
+      int64_t local = 0;
+      for (int x = i0; x < i1; ++x) local += max(e[x], (int64_t)0);
+      int64_t run = warp_inclusive_scan<int64_t>(local) - local;
+      for (int x = i0; x < i1; ++x) {
+        run += max(e[x], (int64_t)0);
+        e[x] = run;
+      }
+    }
+    __syncthreads();
+  }
+
+  const int32_t T = a.bs.size;
+  cp_async_wait_all();  // this thread's positions are in s_pos
+  if (st_n == 1 && q[st_lo] <= t_lo && t_hi <= q[st_lo + 1]) {
+    // Every token of the tile belongs to request st_lo.  A resolved range
+    // whose blocks all lie in [1, num_blocks) becomes a window of positions
+    // [plo, phi) whose slot is p + delta: no division, no lookup.
+    int64_t plo = 0, phi = 0, delta = 0;
+    RangeWindow win;
+#pragma unroll 1
+    for (int k = 0; k < kTokPerThread; ++k) {
+      const int32_t t = base + k * kThreads;
+      if (t >= a.max_num_tokens) break;
+      int64_t slot = kPad;
+      if (t < a.num_tokens) {
+        const int64_t pk = s_pos[k][threadIdx.x];
+        if (pk >= plo && pk < phi) {
+          slot = pk + delta;
+        } else if (pk < 0) {
+          err |= KV_ERR_BAD_POSITION;
+        } else {
+          int64_t lb, off;
+          a.bs.divmod(pk, lb, off);
+          if (win.has(st_lo, lb) || staged_find(s_end, s_beg, s_cnt, rstride, 0, st_lo, lb, win)) {
+            slot = slot_of(win.start + (lb - win.lo), off, T, a.num_blocks, err);
+            // block_size < 2^31, so ends below 2^32 keep hi * T inside int64
+            if (win.start >= 1 && win.start + (win.hi - win.lo) <= a.num_blocks &&
+                win.hi <= (INT64_MAX >> 31)) {
+              plo = win.lo * T;
+              phi = win.hi * T;
+              delta = (win.start - win.lo) * T;
+            }
+          }
+        }
+      }
+      a.slot_mapping[t] = slot;
+    }
+  } else {
+    RangeWindow win;  // this thread's last resolved range
+    ReqSpan last_r;
+#pragma unroll 1
+    for (int k = 0; k < kTokPerThread; ++k) {
+      const int32_t t = base + k * kThreads;
+      if (t >= a.max_num_tokens) break;
+      const int64_t pk = s_pos[k][threadIdx.x];
+      const int r = t < a.num_tokens ? request_of_cached(q, a.num_reqs, t, last_r) : -1;
+      int64_t slot = kPad;
+      if (r >= 0) {
+        if (pk < 0) {
+          err |= KV_ERR_BAD_POSITION;
+        } else {
+          int64_t lb, off;
+          a.bs.divmod(pk, lb, off);
+          bool found = win.has(r, lb);
+          const int j = r - st_lo;
+          if (!found && j >= 0 && j < st_n) {
+            found = staged_find(s_end, s_beg, s_cnt, rstride, j, r, lb, win);
+          } else if (!found) {
+            const int32_t* rs = range_start + (int64_t)r * rstride;
+            const int32_t* rl = range_len + (int64_t)r * rstride;
+            int32_t pre_s[kLanePrefetch], pre_l[kLanePrefetch];
+            lane_prefetch(rs, rl, rstride, vec4, pre_s, pre_l);
+            const int nr = num_ranges[r];
+            if (nr >= 0 && nr <= rstride) found = range_walk(rs, rl, nr, pre_s, pre_l, r, lb, win);
+          }
+          if (found) slot = slot_of(win.start + (lb - win.lo), off, T, a.num_blocks, err);
+        }
+      }
+      a.slot_mapping[t] = slot;
+    }
+  }
+  if (sweep0 < a.num_reqs) {
+    if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
+    for (int r = sweep0 + gridDim.x * blockDim.x; r < a.num_reqs; r += gridDim.x * blockDim.x)
+      if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
+  }
+  report(a.err, err);
+}
+
 // Tokens per thread, measured per map (ncu, cold caches, 262K-2.6M
 // positions).  A wave is 4 resident CTAs per SM.
 // Paged map: 1 while the grid is at most two waves (~311K tokens), else 4
@@ -505,14 +746,36 @@ extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64
   const int tpt = range_tokens_per_thread(max_num_tokens);
   const int grid = grid_for(max_num_tokens, tpt);
   const bool staged = num_reqs + 1 <= kQslSmemMax;
-  const size_t smem = staged && num_reqs > 0 ? sizeof(int32_t) * (num_reqs + 1) : 0;
+  const bool st = staged && num_reqs > 0;
   SlotArgs a{query_start_loc, positions, num_reqs, num_tokens, max_num_tokens,
              BlockDiv::make(block_size), num_blocks, slot_mapping, d_err};
-  const bool st = staged && num_reqs > 0;
   const bool v4 = rows_vec4(range_start, range_len, range_stride);
+  const size_t qsl_smem = st ? sizeof(int32_t) * (num_reqs + 1) : 0;
+  // Descriptor staging pays for large batches (beyond one wave of one token
+  // per thread) whose tiles belong to few requests: on average at least
+  // tile / kStageReqs / 2 tokens per request (prefill batches, long
+  // contexts).  A decode or mixed batch keeps the kernel above (measured:
+  // staging cost a mixed 8432-token batch 1 us, saved 1.7 us at 1M
+  // positions).
+  const int64_t tile = (int64_t)kThreads * tpt;
+  if (tpt > 1 && range_stride > 0 && num_reqs > 0 &&
+      (int64_t)num_tokens * kStageReqs * 2 >= tile * num_reqs) {
+    // staged range ends and starts, then query_start_loc
+    const size_t smem =
+        (size_t)kStageReqs * range_stride * (sizeof(int64_t) + sizeof(int32_t)) + qsl_smem;
+    const size_t static_smem = sizeof(int64_t) * tpt * kThreads + sizeof(int32_t) * kStageReqs;
+    auto kernel = tpt == 4 ? slot_mapping_range_staged_kernel<4>
+                           : slot_mapping_range_staged_kernel<8>;
+    if (smem + static_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return KV_ECUDA;
+    return launch_pdl(kernel, grid, kThreads, smem, stream, a, range_start, range_len,
+                      num_ranges, range_stride, st, v4);
+  }
   auto kernel = tpt == 1   ? slot_mapping_range_kernel<1>
                 : tpt == 4 ? slot_mapping_range_kernel<4>
                            : slot_mapping_range_kernel<8>;
-  return launch_pdl(kernel, grid, kThreads, smem, stream, a, range_start, range_len, num_ranges,
-                    range_stride, st, v4);
+  return launch_pdl(kernel, grid, kThreads, qsl_smem, stream, a, range_start, range_len,
+                    num_ranges, range_stride, st, v4);
 }

@@ -206,6 +206,31 @@ def test_range_equals_paged_with_256_ranges(seed, pad):
     assert np.array_equal(sr, exp) and np.array_equal(sp, exp)
 
 
+# Tiles of 256, 1024 and 2048 tokens (one, four and eight tokens per thread)
+# whose tokens belong to exactly 8 requests (descriptors staged per CTA) or
+# to 9 (each lane walks its own request's ranges); some rows malformed.
+@pytest.mark.parametrize("per_req,pad", [(32, 0), (31, 0), (128, 400_000), (127, 400_000),
+                                         (256, 800_000), (255, 800_000)])
+def test_range_staging_boundary(per_req, pad):
+    rng = np.random.default_rng(3500 + per_req)
+    T, R, S = 16, 40, 12
+    q = (np.arange(R + 1) * per_req).astype(np.int32)
+    N = int(q[-1])
+    rs = rng.integers(1, 5000, size=(R, S)).astype(np.int32)
+    rl = rng.integers(1, 4, size=(R, S)).astype(np.int32)
+    nr = rng.integers(1, S + 1, size=R).astype(np.int32)
+    rl[3, 1] = 0          # an empty range inside a staged row
+    nr[5] = S + 1         # a malformed count
+    rl[11, 0] = -2        # a negative length
+    pos = np.concatenate([rng.permutation(per_req) + int(rng.integers(0, 30)) * T
+                          for _ in range(R)]).astype(np.int64)
+    pos[7] = -4
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N + pad, T, 6000)
+    s, e = run_range(q, pos, rs, rl, nr, N, N + pad, T, 6000)
+    assert e == exp_e
+    assert np.array_equal(s, exp_s)
+
+
 def test_many_requests_qsl_in_global_memory():
     rng = np.random.default_rng(7)
     R, T = 9000, 16
