@@ -1,24 +1,33 @@
 #!/usr/bin/env python3
 """Benchmark of the paged KV-cache hot path on GB300.
 
-One step is one pass of the whole hot path over one synthetic batch.  The
-default workload is the decode step: 256 requests with one new token each,
-contexts U{512..4096}, block size 16, a 40960-block pool, 8 KV heads x 128
-bf16, each request's blocks in 1-4 contiguous ranges.  A step runs
+The headline is the metric's first half on the decode step: 256 requests with
+one new token each, contexts U{512..4096}, block size 16, a 40960-block pool,
+8 KV heads x 128 bf16, each request's blocks in 1-4 contiguous ranges.  One
+step is
 
   1. kv_slot_mapping_paged   (block-table strategy)
   2. kv_slot_mapping_range   (range strategy, same layout, side by side)
   3. kv_cache_write          (the new tokens' K/V rows to their slots)
-  4. kv_cache_gather         (read path: every request's whole context,
-                              through its block table, into packed buffers)
 
-and `value` is new tokens per second over the whole job.  The L2 is flushed
-(a 256 MiB write, then a 256 MiB read) between timed steps, outside the timed
-events.  Rank 0
-prints one JSON line.  `--impl reference` times the CPU oracle instead, on a
-bounded sample of the same workload.  The other workloads (mixed
-prefill+decode over 32 layers, 128K-context gather, hybrid groups) are timed
-per kernel after the headline and reported under "configs".
+captured once in a CUDA graph and replayed, as a serving loop runs its decode
+steps; `value` is new tokens per second over the whole job.  The L2 is
+flushed (a 256 MiB write, then a 256 MiB read) between timed steps, outside
+the timed events.  Beside it, in the same JSON line:
+
+  paged_vs_range   the two strategies' slot map + write, as separate launches
+                   and as the fused calls, each replayed from a CUDA graph;
+  gather_GBps      the metric's second half: the whole-context gather of the
+                   long-context workload (8 x 131072 tokens) through the
+                   permuted table P, with its own roofline (table G and the
+                   range-addressed and bulk-copy gathers under "gather");
+  decode_step_with_gather  the decode step followed by the gather of every
+                   request's whole context (597k rows);
+  e2e              the headline step through the public API from host memory.
+
+Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle on the
+same step instead.  The mixed, long-context and hybrid workloads are timed per
+kernel after the headline and reported under "configs".
 """
 from __future__ import annotations
 
@@ -43,7 +52,9 @@ METRIC = "KV write+slot-map tokens/s and gather GB/s (frac of ~8 TB/s), paged vs
 FLUSH_BYTES = 512 << 20  # two halves of 256 MiB, each twice the 129 MB L2
 DECODE_DESC = ("decode step: 256 requests x 1 new token, context U{512..4096}, block_size 16, "
                "40960-block pool, KV 8x128 bf16 (one layer), 1-4 contiguous ranges per request; "
-               "step = paged slot map + range slot map + KV write + context gather")
+               "step = paged slot map + range slot map + KV write")
+GATHER_DESC = ("long-context gather: 8 requests x 131072 tokens, block_size 16, KV 8x128 bf16, "
+               "whole context of every request into packed K/V buffers (8.59 GB moved)")
 
 
 # --------------------------------------------------------------------------
@@ -142,7 +153,9 @@ def kernel_source_sha(kernel: str) -> str:
     library headers it includes)."""
     files = {"cache_gather_kernel": "kv_cache_gather.cu", "cache_write_kernel": "kv_cache_write.cu",
              "slot_mapping_paged_kernel": "kv_slot_mapping.cu",
-             "slot_mapping_range_kernel": "kv_slot_mapping.cu", "expand_kernel": "kv_expand.cu",
+             "slot_mapping_range_kernel": "kv_slot_mapping.cu",
+             "slot_mapping_range_staged_kernel": "kv_slot_mapping.cu",
+             "expand_kernel": "kv_expand.cu",
              "cache_gather_range_kernel": "kv_cache_gather.cu",
              "table_from_ranges_kernel": "kv_range_table.cu",
              "copy_blocks_kernel": "kv_copy_blocks.cu",
@@ -260,16 +273,19 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
         Launch("cache_write", "cache_write_kernel",
                lambda: kv.kv_cache_write(key, val, kc, vc, slot_p, err=err),
                write_bytes(1, N, N, rb), N),
-        Launch("cache_gather", "cache_gather_kernel",
-               lambda: kv.kv_cache_gather(kc, vc, table, g0, g1, k_out=k_out, v_out=v_out,
-                                          out_rows=rows, err=err),
-               gather_bytes(rows, rb, _touched_blocks(w.gather_start, w.gather_end, T), R), rows),
     ]
+    # the read path after the step: every request's whole context
+    gather = Launch("cache_gather", "cache_gather_kernel",
+                    lambda: kv.kv_cache_gather(kc, vc, table, g0, g1, k_out=k_out, v_out=v_out,
+                                               out_rows=rows, err=err),
+                    gather_bytes(rows, rb, _touched_blocks(w.gather_start, w.gather_end, T), R),
+                    rows)
     if extras:
         table2 = torch.empty_like(table)
         slot_cp = torch.empty_like(slot_p)
         slot_f = torch.empty_like(slot_p)
         launches += [
+            gather,
             Launch("slot_mapping_paged_write", "slot_write_kernel",
                    lambda: kv.kv_slot_mapping_paged_write(qsl, pos, table, T, B, key, val, kc, vc,
                                                           max_num_tokens=n_max,
@@ -300,7 +316,7 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
         ]
     keep = dict(w=w, lay=lay, qsl=qsl, pos=pos, table=table, rs=rs, rl=rl, nr=nr, g0=g0, g1=g1,
                 key=key, val=val, kc=kc, vc=vc, slot_p=slot_p, slot_r=slot_r, err=err,
-                k_out=k_out, v_out=v_out, rows=rows)
+                k_out=k_out, v_out=v_out, rows=rows, gather=gather)
     return Built("decode", DECODE_DESC, launches, N, keep)
 
 
@@ -601,22 +617,26 @@ def kernel_report(built, per, peak):
 # CPU oracle runs (baseline leg and reference arm)
 # --------------------------------------------------------------------------
 
-def oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req):
-    """One oracle pass of the decode step restricted to the first n_req requests."""
-    q = w.qsl[:n_req + 1]
-    n = int(q[-1])
-    pos = w.positions[:n]
-    sp, _ = oracle.slot_mapping_paged(q, pos, lay.table[:n_req], n, n, w.block_size, w.num_blocks)
-    oracle.slot_mapping_range(q, pos, lay.range_start[:n_req], lay.range_len[:n_req],
-                              lay.num_ranges[:n_req], n, n, w.block_size, w.num_blocks)
-    oracle.cache_write(key_h[:, :n], val_h[:, :n], kc_h, vc_h, sp, w.num_blocks, w.block_size)
+def oracle_write_step(oracle, w, lay, kc_h, vc_h, key_h, val_h):
+    """One oracle pass of the headline step on the whole decode batch: both
+    slot maps, then the write of every new token's K/V rows."""
+    n, T, B = w.num_tokens, w.block_size, w.num_blocks
+    sp, _ = oracle.slot_mapping_paged(w.qsl, w.positions, lay.table, n, w.max_num_tokens, T, B)
+    oracle.slot_mapping_range(w.qsl, w.positions, lay.range_start, lay.range_len, lay.num_ranges,
+                              n, w.max_num_tokens, T, B)
+    oracle.cache_write(key_h, val_h, kc_h, vc_h, sp[:n], B, T)
+    return n
+
+
+def oracle_gather_step(oracle, w, lay, kc_h, vc_h, n_req):
+    """The oracle's context gather of the first n_req requests of the decode batch."""
     g0, g1 = w.gather_start[:n_req], w.gather_end[:n_req]
     rows = int((g1.astype(np.int64) - g0).sum())
     ko = np.empty((rows, w.num_kv_heads, w.head_dim), np.uint16)
     vo = np.empty_like(ko)
     oracle.cache_gather(kc_h, vc_h, 0, w.num_blocks, w.block_size, lay.table[:n_req], g0, g1, ko,
                         vo)
-    return n
+    return rows
 
 
 def host_decode_state(wl, seed=1):
@@ -624,8 +644,9 @@ def host_decode_state(wl, seed=1):
     lay = w.layouts["G"]
     rng = np.random.default_rng(99)
     shape = (1, w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
-    kc_h = np.full(shape, 0x3C01, np.uint16)  # contents do not change the oracle's work
-    vc_h = np.full(shape, 0x3C02, np.uint16)
+    # zero-filled host caches: their contents do not change the oracle's work
+    kc_h = np.zeros(shape, np.uint16)
+    vc_h = np.zeros(shape, np.uint16)
     key_h = rng.integers(0, 1 << 16, size=(1, w.num_tokens, w.num_kv_heads, w.head_dim),
                          dtype=np.uint16)
     val_h = rng.integers(0, 1 << 16, size=key_h.shape, dtype=np.uint16)
@@ -633,7 +654,7 @@ def host_decode_state(wl, seed=1):
 
 
 def cpu_baseline(seconds, rounds=5):
-    """The oracle's decode step on one host core, timed in the pages' host-bench
+    """The oracle's headline step on one host core, timed in the pages' host-bench
     manner: `rounds` rounds, one warm-up call per round, then whole steps for
     seconds / rounds; value = mean of the per-round rates, with their stddev."""
     import oracle
@@ -641,11 +662,11 @@ def cpu_baseline(seconds, rounds=5):
     w, lay, kc_h, vc_h, key_h, val_h = host_decode_state(wl)
     rates, steps_total, el_total = [], 0, 0.0
     for _ in range(rounds):
-        oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 8)  # warm-up call
+        oracle_write_step(oracle, w, lay, kc_h, vc_h, key_h, val_h)  # warm-up call
         t0 = time.perf_counter()
         steps, toks = 0, 0
         while True:
-            toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, w.num_reqs)
+            toks += oracle_write_step(oracle, w, lay, kc_h, vc_h, key_h, val_h)
             steps += 1
             el = time.perf_counter() - t0
             if el >= seconds / rounds:
@@ -656,9 +677,9 @@ def cpu_baseline(seconds, rounds=5):
     return {"value": round(statistics.mean(rates), 1),
             "stddev": round(statistics.stdev(rates), 1) if rounds > 1 else 0.0,
             "rounds": rounds, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps_total} whole decode step(s) of the oracle (both slot maps, the "
-                      f"write and the {int((w.gather_end - w.gather_start).sum())}-row context "
-                      f"gather) in {rounds} rounds, single-threaded, {el_total:.1f} s",
+            "sample": f"{steps_total} whole headline steps of the oracle (paged and range slot "
+                      f"maps and the KV write of all 256 decode tokens) in {rounds} rounds, "
+                      f"single-threaded, {el_total:.1f} s",
             "host_cores": os.cpu_count()}
 
 
@@ -730,34 +751,68 @@ def oracle_rows(seconds_cap=4.0):
     timed("expand_kernel_blocks", "entries/s", g.mgr_table.size * 2,
           "hybrid full-attention table 640 x 1024 -> 640 x 2048",
           lambda: oracle.expand_kernel_blocks(g.mgr_table, 32, 16))
+
+    # Large host caches are zero-filled by the allocator, so only the pages a
+    # call touches are ever backed: the blocks a gather reads are written
+    # first (a read of a never-written page would see one shared zero page),
+    # the rows a write fills are backed by its warm-up call.
+    # hybrid full-attention group: one gather call of 64 requests, as issued
+    kt, _ = oracle.expand_kernel_blocks(g.mgr_table, g.mgr_block_size, g.kernel_block_size)
+    kbs, Bk = g.kernel_block_size, g.kernel_num_blocks
+    shape = (1, Bk, kbs, h.num_kv_heads, h.head_dim)
+    kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    g0, g1 = g.gather_start[:64], g.gather_end[:64]
+    rows = int((g1.astype(np.int64) - g0).sum())
+    touched = np.unique(np.concatenate([kt[r, :-(-int(g1[r]) // kbs)] for r in range(64)]))
+    touched = touched[touched > 0]
+    kc[0, touched] = 0x3C01
+    vc[0, touched] = 0x3C02
+    ko = np.empty((rows, h.num_kv_heads, h.head_dim), np.uint16)
+    vo = np.empty_like(ko)
+    timed("cache_gather (hybrid full, one 64-request call)", "rows/s", rows,
+          f"hybrid full-attention group: the first gather call (64 requests, {rows} rows)",
+          lambda: oracle.cache_gather(kc, vc, 0, Bk, kbs, kt[:64], g0, g1, ko, vo))
+    full_rows = int((g.gather_end.astype(np.int64) - g.gather_start).sum())
+    e = out["cache_gather (hybrid full, one 64-request call)"]
+    e["scaled_full_group_s"] = round(full_rows / e["value"], 2)
+    e["scaled"] = f"the whole group ({full_rows} rows in 9 calls) at this call's rate"
+    del kc, vc, ko, vo
+    # mixed prefill+decode: the 32-layer write of all 8432 tokens
+    mw = wl.mixed()
+    L, T, B = mw.num_layers, mw.block_size, mw.num_blocks
+    shape = (L, B, T, mw.num_kv_heads, mw.head_dim)
+    kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    key = np.full((L, mw.num_tokens, mw.num_kv_heads, mw.head_dim), 0x3C03, np.uint16)
+    slots, _ = oracle.slot_mapping_paged(mw.qsl, mw.positions, mw.layouts["G"].table,
+                                         mw.num_tokens, mw.num_tokens, T, B)
+    timed("cache_write (mixed, 32 layers)", "rows/s", L * mw.num_tokens,
+          f"mixed prefill+decode: all {mw.num_tokens} tokens x {L} layers (full size)",
+          lambda: oracle.cache_write(key, key, kc, vc, slots, B, T))
+    del kc, vc, key
     return out
 
 
 def run_reference(args, rk):
-    """The oracle as the reference arm, on bounded samples of the decode step."""
+    """The oracle as the reference arm: the headline step (both slot maps and
+    the write of all 256 decode tokens) on one host core."""
     if not rk.is_main:
         return
     import oracle
     from paged_kv_cache_39_gb300 import workloads as wl
     w, lay, kc_h, vc_h, key_h, val_h = host_decode_state(wl)
-    t0 = time.perf_counter()
-    oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, 4)
-    per_req = (time.perf_counter() - t0) / 4
-    budget = args.reference_seconds / max(1, args.steps + args.warmup)
-    n_req = int(max(1, min(w.num_reqs, budget / max(per_req, 1e-9))))
     for _ in range(args.warmup):
-        oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req)
+        oracle_write_step(oracle, w, lay, kc_h, vc_h, key_h, val_h)
     t0 = time.perf_counter()
     toks = 0
     for _ in range(args.steps):
-        toks += oracle_decode_sample(oracle, w, lay, kc_h, vc_h, key_h, val_h, n_req)
+        toks += oracle_write_step(oracle, w, lay, kc_h, vc_h, key_h, val_h)
     el = time.perf_counter() - t0
     value = toks / el
-    sample = (f"each step: the oracle's decode step on the first {n_req} of 256 requests "
-              f"(both slot maps, write, context gather), single-threaded")
+    sample = ("each step: the oracle's headline step on all 256 requests of the decode batch "
+              "(paged and range slot maps, KV write), single-threaded")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
             "config": {"workload": DECODE_DESC, "parallelism": "host cores, rank 0"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
@@ -767,56 +822,72 @@ def run_reference(args, rk):
     print(json.dumps(line), flush=True)
 
 
+class GraphStep:
+    """`fns` captured once in a CUDA graph (on a side stream first, so lazy
+    set-up stays out of the capture); replay() launches the whole step."""
+
+    def __init__(self, torch, fns):
+        self.torch = torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for fn in fns:
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g):
+            for fn in fns:
+                fn()
+        for _ in range(3):
+            self.g.replay()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.g.replay()
+
+    def times_ms(self, steps, flush_buf):
+        """Device time of each of `steps` replays (CUDA events on the launching
+        stream), L2 flushed between replays outside the events."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush_l2(flush_buf)
+            a.record()
+            self.g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+
 def graph_replay_ms(torch, fns, steps, flush_buf):
-    """Mean device time (ms) of one replay of `fns` captured once in a CUDA
-    graph; L2 flushed between replays, outside the events."""
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for fn in fns:
-            fn()
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for fn in fns:
-            fn()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for a, b in evs:
-        flush_l2(flush_buf)
-        a.record()
-        g.replay()
-        b.record()
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    """Mean device time (ms) of one replay of `fns` captured in a CUDA graph."""
+    g = GraphStep(torch, fns)
+    ms = sum(g.times_ms(steps, flush_buf)) / steps
     del g
     return ms
 
 
-def graph_decode(torch, built, steps, flush_buf):
-    """The same step captured once in a CUDA graph and replayed (how a serving
-    loop runs decode steps)."""
-    ms = graph_replay_ms(torch, [l.fn for l in built.launches], steps, flush_buf)
-    return {"ms_per_step": round(ms, 4), "value": round(built.tokens / (ms * 1e-3), 1),
-            "unit": "tokens/s", "steps": steps,
-            "note": "the four calls captured once in a CUDA graph, one replay per step; "
-                    "L2 flushed between replays"}
+def launch_floor_us(torch, dev, steps, flush_buf):
+    """One replay of a graph holding a single one-element torch kernel: the
+    launch-and-complete floor every latency-bound kernel here sits on."""
+    z = torch.zeros(1, dtype=torch.int32, device=dev)
+    return round(graph_replay_ms(torch, [lambda: z.add_(1)], steps, flush_buf) * 1e3, 2)
 
 
-def write_slotmap_decode(torch, kv, built, kernels, reps, steps, flush_buf, stream, peak):
-    """Slot map + KV write of the decode batch: the separate calls (from the
-    step's per-launch times) against the fused calls (timed here, L2 flushed
-    before every launch), and each pair captured in a CUDA graph."""
+def paged_vs_range(torch, kv, built, steps, reps, flush_buf, stream):
+    """Slot map + KV write of the decode batch by each strategy: the separate
+    slot-map and write launches, and the fused calls, each replayed from one
+    CUDA graph (L2 flushed between replays) and, per launch, timed alone with
+    the L2 flushed before it."""
     k = built.keep
-    w, lay = k["w"], k["lay"]
+    w = k["w"]
     T, B, n_max = w.block_size, w.num_blocks, w.max_num_tokens
     q, p, kc, vc, key, val, err = k["qsl"], k["pos"], k["kc"], k["vc"], k["key"], k["val"], k["err"]
     slot_p, slot_r = k["slot_p"], k["slot_r"]
     slot_f = torch.empty_like(slot_p)
+    sep = {l.name: l.fn for l in built.launches}
     fused = {
         "paged": lambda: kv.kv_slot_mapping_paged_write(q, p, k["table"], T, B, key, val, kc, vc,
                                                         max_num_tokens=n_max, slot_mapping=slot_f,
@@ -825,68 +896,162 @@ def write_slotmap_decode(torch, kv, built, kernels, reps, steps, flush_buf, stre
                                                         key, val, kc, vc, max_num_tokens=n_max,
                                                         slot_mapping=slot_f, err=err),
     }
-    sep = {l.name: l.fn for l in built.launches}
-    fb = Built("fused", "", [Launch("slot_mapping_paged_write", "slot_write_kernel",
-                                    fused["paged"], 0, w.num_tokens),
-                             Launch("slot_mapping_range_write", "slot_write_kernel",
-                                    fused["range"], 0, w.num_tokens)], w.num_tokens, k)
-    for _ in range(3):
-        for l in fb.launches:
-            l.fn()
-    per = time_each(torch, fb, reps, flush_buf, stream)
-    us_f = {n: sum(t) / len(t) * 1e3 for n, t in zip(("paged", "range"), per)}
-    tw = kernels["cache_write"]["us"]
-    us_sep = {"paged": kernels["slot_mapping_paged"]["us"] + tw,
-              "range": kernels["slot_mapping_range"]["us"] + tw}
+    write_r = lambda: kv.kv_cache_write(key, val, kc, vc, slot_r, err=err)  # noqa: E731
     graphs = {
         "paged": [sep["slot_mapping_paged"], sep["cache_write"]],
-        "range": [sep["slot_mapping_range"],
-                  lambda: kv.kv_cache_write(key, val, kc, vc, slot_r, err=err)],
+        "range": [sep["slot_mapping_range"], write_r],
         "paged_fused": [fused["paged"]],
         "range_fused": [fused["range"]],
     }
     g_us = {n: graph_replay_ms(torch, fns, steps, flush_buf) * 1e3 for n, fns in graphs.items()}
-    n = built.tokens
+    per_launch = Built("pvr", "", [
+        Launch("slot_mapping_paged", "", sep["slot_mapping_paged"], 0),
+        Launch("slot_mapping_range", "", sep["slot_mapping_range"], 0),
+        Launch("cache_write", "", sep["cache_write"], 0),
+        Launch("slot_mapping_paged_write", "", fused["paged"], 0),
+        Launch("slot_mapping_range_write", "", fused["range"], 0)], 0, k)
+    per = time_each(torch, per_launch, reps, flush_buf, stream)
+    us = {l.name: round(sum(t) / len(t) * 1e3, 2) for l, t in zip(per_launch.launches, per)}
+    torch.cuda.synchronize()
     if not torch.equal(slot_f, slot_r) or not torch.equal(slot_p, slot_r):
         raise RuntimeError("fused and separate slot mappings differ")
+    n = built.tokens
     return {
-        "paged": round(n / (us_sep["paged"] * 1e-6), 1),
-        "range": round(n / (us_sep["range"] * 1e-6), 1),
-        "paged_fused": round(n / (us_f["paged"] * 1e-6), 1),
-        "range_fused": round(n / (us_f["range"] * 1e-6), 1),
-        "us": {"paged": round(us_sep["paged"], 2), "range": round(us_sep["range"], 2),
-               "paged_fused": round(us_f["paged"], 2), "range_fused": round(us_f["range"], 2)},
-        "graph_replay_us": {n_: round(v, 2) for n_, v in g_us.items()},
-        "graph_replay_tokens_per_s": {n_: round(n / (v * 1e-6), 1) for n_, v in g_us.items()},
-        "note": "paged/range: the slot-map launch plus the write launch, each timed with L2 "
-                "flushed before it; *_fused: kv_slot_mapping_{paged,range}_write, one launch, "
-                "timed the same way; graph_replay: each pair captured in one CUDA graph, L2 "
-                "flushed between replays",
+        "tokens_per_s": {name: round(n / (v * 1e-6), 1) for name, v in g_us.items()},
+        "graph_replay_us": {name: round(v, 2) for name, v in g_us.items()},
+        "range_over_paged": {"separate": round(g_us["range"] / g_us["paged"], 3),
+                             "fused": round(g_us["range_fused"] / g_us["paged_fused"], 3)},
+        "per_launch_us": us,
+        "replays": steps, "per_launch_reps": reps,
+        "note": "paged/range: that strategy's slot-map launch then the write launch, captured "
+                "in one CUDA graph; *_fused: kv_slot_mapping_{paged,range}_write, one launch "
+                "in a graph; each replayed with the L2 flushed between replays.  per_launch_us: "
+                "each call alone, L2 flushed before it (CUDA events tick in 2.05 us steps; the "
+                "means are over all reps)",
     }
+
+
+def gather_long(torch, kv, wl, dev, reps, flush_buf, stream, peak, same_run_copy, small=False):
+    """The metric's second half: the whole-context gather of the long-context
+    workload through the permuted table P (the general case) and the packed
+    ranges' table G, the range-addressed and the bulk-copy gathers beside it."""
+    w = wl.long_context(num_reqs=2 if small else 8)
+    T, B, H, D = w.block_size, w.num_blocks, w.num_kv_heads, w.head_dim
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    tp, tg = t(w.layouts["P"].table), t(w.layouts["G"].table)
+    lg = w.layouts["G"]
+    rs, rl, nr = t(lg.range_start), t(lg.range_len), t(lg.num_ranges)
+    g0, g1 = t(w.gather_start), t(w.gather_end)
+    kc = wl.bf16_normal((1, B, T, H, D), 31, dev)
+    vc = wl.bf16_normal((1, B, T, H, D), 32, dev)
+    rows = w.num_tokens
+    k_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    R = w.num_reqs
+    gb = gather_bytes(rows, w.row_bytes, _touched_blocks(w.gather_start, w.gather_end, T), R)
+    gr = rows * w.row_bytes * 4 + int(lg.num_ranges.sum()) * 8 + R * 12
+    b = Built("gather", GATHER_DESC, [
+        Launch("cache_gather[P]", "cache_gather_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tp, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err), gb, rows),
+        Launch("cache_gather[G]", "cache_gather_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err), gb, rows),
+        Launch("cache_gather_range[G]", "cache_gather_range_kernel",
+               lambda: kv.kv_cache_gather_range(kc, vc, rs, rl, nr, g0, g1, k_out=k_out,
+                                                v_out=v_out, out_rows=rows, err=err), gr, rows),
+        Launch("cache_gather_bulk[P]", "cache_gather_bulk_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tp, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err, bulk=True), gb, rows),
+        Launch("cache_gather_bulk[G]", "cache_gather_bulk_kernel",
+               lambda: kv.kv_cache_gather(kc, vc, tg, g0, g1, k_out=k_out, v_out=v_out,
+                                          out_rows=rows, err=err, bulk=True), gb, rows),
+    ], rows, dict(err=err))
+    for _ in range(3):
+        for l in b.launches:
+            l.fn()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"long-context gathers reported data errors: {int(err.item())}")
+    per = time_each(torch, b, reps, flush_buf, stream)
+    rep = kernel_report(b, per, peak[0])
+    p = b.launches[0]
+    avg_ms = sum(per[0]) / len(per[0])
+    achieved = p.alg_bytes / (avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(p.kernel, "long")
+    if traffic is not None and small:
+        traffic = None
+    out = {"GBps": round(achieved, 1), "workload": GATHER_DESC + (" [small]" if small else ""),
+           "kernels": rep,
+           "roofline": {"bound": "hbm", "kernel": p.kernel + " (table P)",
+                        "achieved": round(achieved, 1), "peak": peak[0],
+                        "peak_kind": f"{peak[1]} hbm_gbs (copy, read+write)", "unit": "GB/s",
+                        "frac": round(achieved / peak[0], 4), "traffic": traffic,
+                        "alg_bytes_per_launch": int(p.alg_bytes),
+                        "avg_launch_us": round(avg_ms * 1e3, 2),
+                        "same_run_copy_GBps": same_run_copy,
+                        "frac_of_same_run_copy": round(achieved / same_run_copy, 4),
+                        "frac_of_8TBps": round(achieved / 8000.0, 4)},
+           "l2": "inputs and outputs (4.3 GB each way) far larger than L2; flushed before "
+                 "every launch as well", "reps": reps}
+    del b, kc, vc, k_out, v_out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def decode_step_with_gather(torch, built, steps, flush_buf, stream, peak, args):
+    """The decode step followed by the read path: the three calls of the
+    headline step, then the gather of every request's whole context (597k
+    rows, 4.9 GB moved), timed per launch within each step and replayed from
+    one CUDA graph."""
+    b = Built("decode+gather", "", built.launches + [built.keep["gather"]], built.tokens,
+              built.keep)
+    step_ms, per = time_steps(torch, b, steps, flush_buf, stream)
+    rep = kernel_report(b, per, peak[0])
+    g = b.launches[-1]
+    avg_ms = sum(per[-1]) / len(per[-1])
+    achieved = g.alg_bytes / (avg_ms * 1e-3) / 1e9
+    ms = sum(step_ms) / len(step_ms)
+    g_ms = graph_replay_ms(torch, [l.fn for l in b.launches], steps, flush_buf)
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(b.tokens / (ms * 1e-3), 1),
+            "graph_ms_per_step": round(g_ms, 4),
+            "graph_tokens_per_s": round(b.tokens / (g_ms * 1e-3), 1),
+            "steps": steps, "kernels": rep,
+            "gather_roofline": {"bound": "hbm", "kernel": g.kernel,
+                                "achieved": round(achieved, 1), "peak": peak[0],
+                                "unit": "GB/s", "frac": round(achieved / peak[0], 4),
+                                "traffic": profiled_traffic(g.kernel, "decode"),
+                                "alg_bytes_per_launch": int(g.alg_bytes),
+                                "avg_launch_us": round(avg_ms * 1e3, 2)},
+            "note": "per-launch events inside each step (L2 flushed between steps); graph: the "
+                    "four calls in one CUDA graph"}
 
 
 # --------------------------------------------------------------------------
 # end to end through the public API with host buffers
 # --------------------------------------------------------------------------
 
-def e2e_decode(torch, kv, built, steps, flush_buf, stream):
-    """The decode step through the public API from host memory: every step
-    uploads its inputs from pinned host memory (packed, one copy), runs the
-    four calls, and reads back both slot mappings and the error word.
+def e2e_step(torch, kv, built, steps, flush_buf, stream):
+    """The headline step through the public API from host memory: every step
+    uploads its inputs from pinned host memory (packed, one copy), replays the
+    three prepared calls from a CUDA graph, and reads back both slot mappings
+    and the error word.
 
-    Measured the way a serving loop runs it: two sets of device buffers, the
-    upload of step k+1 on a copy stream while step k computes, and the host
-    consuming step k's read-back (checking its error word) while step k+1
-    runs; value = steps / wall time.  The same calls with every step
-    synchronised on its own (upload, calls, read-back, wait) are reported as
-    `sync_ms_per_step`."""
+    Measured the way a serving loop runs it: two sets of device buffers (each
+    with its own graph), the upload of step k+1 on a copy stream while step k
+    computes, and the host consuming step k's read-back (checking its error
+    word and a slot) while step k+1 runs; value = steps / wall time.  The same
+    step synchronised on its own (upload, replay, read-back, wait) is reported
+    as `sync_ms_per_step`."""
     k = built.keep
     w, lay = k["w"], k["lay"]
     dev = k["qsl"].device
-    names = ["qsl", "pos", "table", "rs", "rl", "nr", "g0", "g1", "key", "val"]
+    names = ["qsl", "pos", "table", "rs", "rl", "nr", "key", "val"]
     host_src = {"qsl": w.qsl, "pos": w.positions, "table": lay.table, "rs": lay.range_start,
-                "rl": lay.range_len, "nr": lay.num_ranges, "g0": w.gather_start,
-                "g1": w.gather_end, "key": k["key"].cpu(), "val": k["val"].cpu()}
+                "rl": lay.range_len, "nr": lay.num_ranges, "key": k["key"].cpu(),
+                "val": k["val"].cpu()}
     # one pinned staging buffer, each input at a 256-byte offset
     offs, total = {}, 0
     for n in names:
@@ -898,15 +1063,16 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
         src = host_src[n]
         src = torch.from_numpy(np.ascontiguousarray(src)) if isinstance(src, np.ndarray) else src
         h_stage[offs[n]:offs[n] + nbytes].copy_(src.contiguous().view(-1).view(torch.uint8))
-    T, B, n_max, rows = w.block_size, w.num_blocks, w.max_num_tokens, k["rows"]
+    T, B, n_max = w.block_size, w.num_blocks, w.max_num_tokens
     n_slot = k["slot_p"].numel()
     out_bytes = 2 * n_slot * 8 + 256
 
     class Slot:
-        """One set of device buffers: inputs, packed outputs, prepared calls."""
+        """One set of device buffers: inputs, packed outputs, the step's graph."""
 
         def __init__(self):
             self.d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+            self.d_stage.copy_(h_stage)
             d = {n: self.d_stage[offs[n]:offs[n] + k[n].numel() * k[n].element_size()]
                  .view(k[n].dtype).view(k[n].shape) for n in names}
             # outputs: both slot mappings and the error word, read back with one copy
@@ -915,8 +1081,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
             slot_p = self.d_out[:n_slot * 8].view(torch.int64)
             slot_r = self.d_out[n_slot * 8:2 * n_slot * 8].view(torch.int64)
             err = self.d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)
-            # validated once; each step relaunches with the cached pointers
-            self.calls = [
+            # validated once; the graph replays them with the cached pointers
+            calls = [
                 kv.kv_slot_mapping_paged(d["qsl"], d["pos"], d["table"], T, B,
                                          max_num_tokens=n_max, slot_mapping=slot_p, err=err,
                                          prepare=True),
@@ -925,10 +1091,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
                                          prepare=True),
                 kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=err,
                                   prepare=True),
-                kv.kv_cache_gather(k["kc"], k["vc"], d["table"], d["g0"], d["g1"],
-                                   k_out=k["k_out"], v_out=k["v_out"], out_rows=rows, err=err,
-                                   prepare=True),
             ]
+            self.graph = GraphStep(torch, calls)
             self.ev_in, self.ev_used, self.ev_out = (torch.cuda.Event(), torch.cuda.Event(),
                                                      torch.cuda.Event())
 
@@ -937,6 +1101,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
 
     slots = [Slot(), Slot()]
     copy_stream = torch.cuda.Stream(device=dev)
+    probe = int(np.argmax(w.positions >= 0))
+    exp_probe = int(k["slot_p"][probe].item())
 
     def enqueue(i, first):
         sl = slots[i]
@@ -946,8 +1112,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
             sl.d_stage.copy_(h_stage, non_blocking=True)
             sl.ev_in.record(copy_stream)
         stream.wait_event(sl.ev_in)
-        for c in sl.calls:
-            c()
+        sl.d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].zero_()
+        sl.graph.replay()
         sl.ev_used.record(stream)
         sl.h_out.copy_(sl.d_out, non_blocking=True)
         sl.ev_out.record(stream)
@@ -956,6 +1122,8 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
         slots[i].ev_out.synchronize()
         if slots[i].error_word() != 0:
             raise RuntimeError("end-to-end step reported data errors")
+        if int(slots[i].h_out[:n_slot * 8].view(torch.int64)[probe]) != exp_probe:
+            raise RuntimeError("end-to-end step read back a wrong slot")
 
     def run(n):
         for s in range(n):
@@ -970,15 +1138,14 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
     run(steps)
     wall = time.perf_counter() - t0
 
-    # every step on its own: upload, calls, read-back, wait (L2 flushed before)
+    # every step on its own: upload, replay, read-back, wait (L2 flushed before)
     times = []
     for s in range(min(steps, 200)):
         flush_l2(flush_buf)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         slots[0].d_stage.copy_(h_stage, non_blocking=True)
-        for c in slots[0].calls:
-            c()
+        slots[0].graph.replay()
         slots[0].h_out.copy_(slots[0].d_out, non_blocking=True)
         stream.synchronize()
         times.append(time.perf_counter() - t1)
@@ -990,17 +1157,18 @@ def e2e_decode(torch, kv, built, steps, flush_buf, stream):
                 or not torch.equal(back_r, k["slot_r"].cpu())):
             raise RuntimeError("end-to-end read-back differs from the device-resident step")
     ms = wall / steps * 1e3
+    del slots
     return {"value": round(built.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(out_bytes),
             "ms_per_step": round(ms, 4), "steps": steps,
-            "sync_ms_per_step": round(statistics.median(times) * 1e3, 3),
-            "note": "wall time over all steps: each step uploads its packed inputs from pinned "
-                    "host memory (copy stream, double-buffered so step k+1's upload overlaps "
-                    "step k), runs the four prepared calls and copies both slot mappings and "
-                    "the error word back, which the host checks one step later; steps run "
-                    "back to back without an L2 flush (each moves 4.9 GB, far more than L2); "
-                    "sync_ms_per_step: median of the same step run alone and waited for, L2 "
-                    "flushed before it"}
+            "sync_ms_per_step": round(statistics.median(times) * 1e3, 4),
+            "note": "wall time over all steps: each step uploads its packed inputs (positions, "
+                    "query_start_loc, block table, range descriptors, new K/V rows) from pinned "
+                    "host memory on a copy stream, double-buffered so step k+1's upload "
+                    "overlaps step k, replays the three prepared calls from a CUDA graph and "
+                    "copies both slot mappings and the error word back, which the host checks "
+                    "one step later; sync_ms_per_step: median of the same step run alone and "
+                    "waited for, L2 flushed before it"}
 
 
 # --------------------------------------------------------------------------
@@ -1018,7 +1186,6 @@ def main():
                     help="shrink the workload (profiling captures); not a bench line")
     ap.add_argument("--no-detail", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--detail-reps", type=int, default=10)
     args = ap.parse_args()
     args.steps = max(1, args.steps)
@@ -1040,7 +1207,106 @@ def main():
     stream = torch.cuda.current_stream(dev)
     peak, peak_kind = load_peaks()
     flush_buf = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    if args.workload != "decode":
+        return profile_run(torch, kv, wl, dev, args, rk, flush_buf, stream, peak, kdist)
 
+    built = build_decode(torch, kv, wl, dev, small=args.small)
+    for _ in range(args.warmup):
+        flush_l2(flush_buf)
+        for l in built.launches:
+            l.fn()
+    torch.cuda.synchronize()
+    if int(built.keep["err"].item()) != 0:
+        raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
+    step = GraphStep(torch, [l.fn for l in built.launches])
+
+    with ClockSampler() as clocks:
+        kdist.barrier(dev)
+        torch.cuda.synchronize()
+        step_ms = step.times_ms(args.steps, flush_buf)
+        torch.cuda.synchronize()
+        kdist.barrier(dev)
+    if int(built.keep["err"].item()) != 0:
+        raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
+    ms_per_step = sum(step_ms) / len(step_ms)
+    ms_max = kdist.max_over_ranks(ms_per_step, dev)
+    value = built.tokens * rk.world_size / (ms_max * 1e-3)
+    del step
+
+    # the step's kernels one by one (L2 flushed before each) for the roofline
+    reps = min(max(args.steps, 100), 1000)
+    per = time_each(torch, built, reps, flush_buf, stream)
+    kernels = kernel_report(built, per, peak)
+    dom_i = max(range(len(built.launches)), key=lambda i: sum(per[i]))
+    dom = built.launches[dom_i]
+    dom_avg_ms = sum(per[dom_i]) / len(per[dom_i])
+    achieved = dom.alg_bytes / (dom_avg_ms * 1e-3) / 1e9
+    floor_us = launch_floor_us(torch, dev, min(max(args.steps, 100), 1000), flush_buf)
+    roofline = {"bound": "hbm", "kernel": dom.kernel, "achieved": round(achieved, 1),
+                "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, read+write)",
+                "unit": "GB/s", "frac": round(achieved / peak, 6),
+                "traffic": profiled_traffic(dom.kernel, "decode"),
+                "alg_bytes_per_launch": int(dom.alg_bytes),
+                "avg_launch_us": round(dom_avg_ms * 1e3, 2),
+                "launch_floor_us": floor_us,
+                "regime": "latency: 256 tokens move a few KB to 2 MB per kernel, so every "
+                          "kernel of the step is a chain of dependent DRAM round trips on top "
+                          "of the launch; launch_floor_us is one replay of a graph holding a "
+                          "single one-element kernel",
+                "timing": f"each call alone, L2 flushed before it, mean of {reps} launches"}
+    same_run_copy = copy_ceiling(torch, dev, flush_buf, reps=5)["torch_copy_GBps_median"]
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": rk.world_size, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "payload": "bf16 bits copied",
+            "data": "synthetic",
+            "config": {"workload": built.desc + (" [small]" if args.small else ""),
+                       "l2": "flushed between timed steps outside the events (256 MiB written, then "
+                             "another 256 MiB read)",
+                       "timing": "the step's three calls captured once in a CUDA graph, one "
+                                 "replay per step, CUDA events around each replay",
+                       "parallelism": "replicas" if rk.world_size > 1 else "single GPU",
+                       "per_gpu_tokens_per_step": built.tokens},
+            "kernels": kernels, "roofline": roofline,
+            "gpu_launches": args.steps * len(built.launches),
+            "clocks": clocks.summary()}
+    line["paged_vs_range"] = paged_vs_range(torch, kv, built, min(max(args.steps, 500), 2000),
+                                            reps, flush_buf, stream)
+    gather = gather_long(torch, kv, wl, dev, max(args.detail_reps, 5), flush_buf, stream,
+                         (peak, peak_kind), same_run_copy, small=args.small)
+    line["gather_GBps"] = gather["GBps"]
+    line["gather"] = gather
+    line["decode_step_with_gather"] = decode_step_with_gather(
+        torch, built, min(args.steps, 500), flush_buf, stream, (peak, peak_kind), args)
+    e2e = e2e_step(torch, kv, built, min(max(args.steps, 500), 5000), flush_buf, stream)
+    if rk.world_size > 1:
+        # whole job, like `value`: every rank's tokens over the slowest rank's step
+        kdist.barrier(dev)
+        e2e_ms = kdist.max_over_ranks(e2e["ms_per_step"], dev)
+        e2e["per_gpu_value"] = e2e["value"]
+        e2e["ms_per_step"] = round(e2e_ms, 4)
+        e2e["value"] = round(built.tokens * rk.world_size / (e2e_ms * 1e-3), 1)
+    line["e2e"] = e2e
+
+    if rk.is_main and rk.world_size == 1:
+        if args.cpu_seconds > 0:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if not args.no_detail:
+            built = None
+            torch.cuda.empty_cache()
+            line["configs"] = detail(torch, kv, wl, dev, args, flush_buf, stream, peak)
+            if args.cpu_seconds > 0:
+                line["oracle_rows"] = oracle_rows()
+    if rk.is_main:
+        print(json.dumps(line), flush=True)
+    kdist.finalize()
+
+
+def profile_run(torch, kv, wl, dev, args, rk, flush_buf, stream, peak, kdist):
+    """`--workload X` (X not the decode step): the workload's launches in
+    order, per-launch events, L2 flushed between steps.  For profiler captures
+    and kernel A/B runs; the line is marked as not a bench line."""
     built = BUILDERS[args.workload](torch, kv, wl, dev, small=args.small)
     for _ in range(args.warmup):
         flush_l2(flush_buf)
@@ -1049,77 +1315,11 @@ def main():
     torch.cuda.synchronize()
     if int(built.keep["err"].item()) != 0:
         raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
-
-    with ClockSampler() as clocks:
-        kdist.barrier(dev)
-        torch.cuda.synchronize()
-        step_ms, per = time_steps(torch, built, args.steps, flush_buf, stream)
-        torch.cuda.synchronize()
-        kdist.barrier(dev)
-    # the device copy ceiling on this GPU now: box-to-box HBM differences of a
-    # few percent make the same-run ratio the fair one to compare runs with
-    same_run_copy = copy_ceiling(torch, dev, flush_buf, reps=5)["torch_copy_GBps_median"]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    ms_max = kdist.max_over_ranks(ms_per_step, dev)
-    value = built.tokens * rk.world_size / (ms_max * 1e-3)
-    kernels = kernel_report(built, per, peak)
-
-    # dominant kernel of the step
-    dom_i = max(range(len(built.launches)), key=lambda i: sum(per[i]))
-    dom = built.launches[dom_i]
-    dom_avg_ms = sum(per[dom_i]) / len(per[dom_i])
-    achieved = dom.alg_bytes / (dom_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(dom.kernel, args.workload)
-    roofline = {"bound": "hbm", "kernel": dom.kernel, "achieved": round(achieved, 1),
-                "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, read+write)",
-                "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "alg_bytes_per_launch": int(dom.alg_bytes),
-                "avg_launch_us": round(dom_avg_ms * 1e3, 2),
-                "same_run_copy_GBps": same_run_copy,
-                "frac_of_same_run_copy": round(achieved / same_run_copy, 4)}
-
-    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
-            "n_gpus": rk.world_size, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int64", "payload": "bf16 bits copied",
-            "data": "synthetic",
-            "config": {"workload": built.desc + (" [small]" if args.small else ""),
-                       "l2": "flushed between timed steps outside the events (256 MiB written, then "
-                                    "another 256 MiB read)",
-                       "parallelism": "replicas" if rk.world_size > 1 else "single GPU",
-                       "per_gpu_tokens_per_step": built.tokens},
-            "kernels": kernels, "roofline": roofline,
-            "gpu_launches": args.steps * sum(l.launches for l in built.launches),
-            "clocks": clocks.summary()}
-    if built.name == "decode":
-        line["write_slotmap_tokens_per_s"] = write_slotmap_decode(
-            torch, kv, built, kernels, args.detail_reps * 10, min(args.steps, 500), flush_buf,
-            stream, peak)
-        line["gather_GBps"] = kernels["cache_gather"]["GB/s"]
-        line["graph"] = graph_decode(torch, built, min(args.steps, 500), flush_buf)
-        if rk.world_size > 1:
-            g_ms = kdist.max_over_ranks(line["graph"]["ms_per_step"], dev)
-            line["graph"]["ms_per_step"] = round(g_ms, 4)
-            line["graph"]["value"] = round(built.tokens * rk.world_size / (g_ms * 1e-3), 1)
-        e2e = e2e_decode(torch, kv, built, min(args.steps, 1000), flush_buf, stream)
-        if rk.world_size > 1:
-            # whole job, like `value`: every rank's tokens over the slowest rank's step
-            kdist.barrier(dev)
-            e2e_ms = kdist.max_over_ranks(e2e["ms_per_step"], dev)
-            e2e["per_gpu_value"] = e2e["value"]
-            e2e["ms_per_step"] = round(e2e_ms, 4)
-            e2e["value"] = round(built.tokens * rk.world_size / (e2e_ms * 1e-3), 1)
-        line["e2e"] = e2e
-
-    if rk.is_main and rk.world_size == 1:
-        if args.workload == "decode" and args.cpu_seconds > 0:
-            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
-        if not args.no_detail and args.workload == "decode":
-            built = None
-            torch.cuda.empty_cache()
-            line["configs"] = detail(torch, kv, wl, dev, args, flush_buf, stream, peak)
-            if args.cpu_seconds > 0:
-                line["oracle_rows"] = oracle_rows()
+    step_ms, per = time_steps(torch, built, args.steps, flush_buf, stream)
+    line = {"not_a_bench_line": f"--workload {args.workload}", "workload": built.desc +
+            (" [small]" if args.small else ""), "steps": args.steps,
+            "ms_per_step": round(sum(step_ms) / len(step_ms), 4),
+            "kernels": kernel_report(built, per, peak)}
     if rk.is_main:
         print(json.dumps(line), flush=True)
     kdist.finalize()
