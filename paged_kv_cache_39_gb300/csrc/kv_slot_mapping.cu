@@ -403,8 +403,9 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
 // The grid-wide sweep over every descriptor row sets BAD_RANGE as in the
 // kernel above.
 
-constexpr int kStageReqs = 8;  // requests a CTA stages (one warp each for the scan)
-static_assert(kStageReqs == kThreads / 32, "one warp scans each staged request");
+constexpr int kStageReqs = 8;  // requests a CTA stages (one warp each)
+constexpr int kStageCap = 32;  // descriptors staged per request (one per lane)
+static_assert(kStageReqs == kThreads / 32, "one warp stages each request");
 
 // Logical block lb of request r by a walk of its descriptor row in global
 // memory (pre_*: its first kLanePrefetch descriptors, nr: its count).
@@ -437,21 +438,71 @@ __device__ __forceinline__ bool range_walk(const int32_t* __restrict__ rs,
   return false;
 }
 
+// The same walk without the prefetched head (fewer registers, for tiles
+// that could not be staged).
+__device__ __forceinline__ bool range_walk_plain(const int32_t* __restrict__ rs,
+                                                 const int32_t* __restrict__ rl, int nr, int r,
+                                                 int64_t lb, RangeWindow& win) {
+  int64_t cum = 0;
+  for (int i = 0; i < nr; ++i) {
+    const int64_t len = max(rl[i], 0);
+    if (lb < cum + len) {
+      win = RangeWindow{r, cum, cum + len, rs[i]};
+      return true;
+    }
+    cum += len;
+  }
+  return false;
+}
+
 // Staged row j (counts in s_cnt, range ends in s_end, starts in s_beg):
 // the range holding logical block lb, or false when no range does.
-__device__ __forceinline__ bool staged_find(const int64_t* s_end, const int32_t* s_beg,
-                                            const int32_t* s_cnt, int32_t rstride, int j,
-                                            int r, int64_t lb, RangeWindow& win) {
+__device__ __forceinline__ bool staged_find(const int64_t (*s_end)[kStageCap],
+                                            const int32_t (*s_beg)[kStageCap],
+                                            const int32_t* s_cnt, int j, int r, int64_t lb,
+                                            RangeWindow& win) {
   const int n = s_cnt[j];
-  const int64_t* e = s_end + (size_t)j * rstride;
+  const int64_t* e = s_end[j];
   if (n <= 0 || lb >= e[n - 1]) return false;
   int lo = 0, hi = n - 1;
   while (lo < hi) {  // first range whose end passes lb
     const int mid = (lo + hi) >> 1;
     if (e[mid] > lb) hi = mid; else lo = mid + 1;
   }
-  win = RangeWindow{r, lo > 0 ? e[lo - 1] : 0, e[lo], s_beg[(size_t)j * rstride + lo]};
+  win = RangeWindow{r, lo > 0 ? e[lo - 1] : 0, e[lo], s_beg[j][lo]};
   return true;
+}
+
+// Positions [plo, phi) of one range whose blocks are all valid: slot p + delta.
+struct PosWindow {
+  int64_t plo = 0, phi = 0, delta = 0;
+  __device__ __forceinline__ bool has(int64_t p) const { return p >= plo && p < phi; }
+};
+
+// Slot of position p of request r (the staged row 0) when p is outside the
+// position window: resolve its range, and make that range the window when
+// all its blocks are valid.
+__device__ __forceinline__ int64_t window_miss(int64_t p, const SlotArgs& a,
+                                               const int64_t (*s_end)[kStageCap],
+                                               const int32_t (*s_beg)[kStageCap],
+                                               const int32_t* s_cnt, int r, RangeWindow& win,
+                                               PosWindow& pw, uint32_t& err) {
+  if (p < 0) {
+    err |= KV_ERR_BAD_POSITION;
+    return kPad;
+  }
+  const int64_t T = a.bs.size;
+  int64_t lb, off;
+  a.bs.divmod(p, lb, off);
+  if (!win.has(r, lb) && !staged_find(s_end, s_beg, s_cnt, 0, r, lb, win)) return kPad;
+  // block_size < 2^31, so ends below 2^32 keep hi * T inside int64
+  if (win.start >= 1 && win.start + (win.hi - win.lo) <= a.num_blocks &&
+      win.hi <= (INT64_MAX >> 31)) {
+    pw.plo = win.lo * T;
+    pw.phi = win.hi * T;
+    pw.delta = (win.start - win.lo) * T;
+  }
+  return slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err);
 }
 
 // At most 64 registers: four CTAs per SM keep the grid within one wave
@@ -465,13 +516,9 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
                                  bool qsl_in_smem, bool vec4) {
   pdl_allow_next();
   pdl_wait();
-  // dynamic shared memory: the staged range ends (int64) and starts
-  // (int32), kStageReqs rows of rstride each; then query_start_loc
-  extern __shared__ int64_t s_dyn[];
-  const size_t staged_entries = (size_t)kStageReqs * rstride;
-  int64_t* s_end = s_dyn;
-  int32_t* s_beg = reinterpret_cast<int32_t*>(s_end + staged_entries);
-  int32_t* s_qsl = s_beg + staged_entries;
+  extern __shared__ int32_t s_qsl[];
+  __shared__ int64_t s_end[kStageReqs][kStageCap];  // staged range ends
+  __shared__ int32_t s_beg[kStageReqs][kStageCap];  // staged range starts
   // positions staged per thread in shared memory: the token loops stay
   // rolled (one copy of their search paths keeps the instruction footprint
   // small) and no register holds a position while it is in flight; only the
@@ -514,42 +561,28 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
     }
   }
   if (st_n > 0) {
-    // thread i loads descriptor i of every staged row, all loads in flight
-    // together, straight into shared memory (lengths as raw int64)
-    const int i = threadIdx.x;
-    if (i < st_n) s_cnt[i] = num_ranges[st_lo + i];
-    if (i < rstride) {
-#pragma unroll 2
-      for (int j = 0; j < kStageReqs; ++j) {
-        if (j < st_n) {
-          const int64_t row = (int64_t)(st_lo + j) * rstride;
-          s_beg[(size_t)j * rstride + i] = range_start[row + i];
-          s_end[(size_t)j * rstride + i] = range_len[row + i];
-        }
-      }
-    }
-    __syncthreads();
-    // warp j scans row j: its count is checked (-1: malformed, all PAD),
-    // lengths <= 0 count as empty, lane l sums a contiguous share of the
-    // row's first `count` entries, a warp scan of the shares, then the
-    // running sums (the range ends) are written back in place
+    // warp j stages row st_lo + j: the count and the first kStageCap
+    // descriptors (one per lane) in one round trip, the lengths scanned into
+    // range ends (lengths <= 0 count as empty; a malformed count -1, all PAD)
     if (wid < st_n) {
-      const int raw = s_cnt[wid];
-      const int n = (raw >= 0 && raw <= rstride) ? raw : -1;
-      __syncwarp();
-      if (lane == 0) s_cnt[wid] = n;
-      int64_t* e = s_end + (size_t)wid * rstride;
-      const int per = (max(n, 0) + 31) / 32;
-      const int i0 = lane * per, i1 = min(max(n, 0), i0 + per);
-      int64_t local = 0;
-      for (int x = i0; x < i1; ++x) local += max(e[x], (int64_t)0);
-      int64_t run = warp_inclusive_scan<int64_t>(local) - local;
-      for (int x = i0; x < i1; ++x) {
-        run += max(e[x], (int64_t)0);
-        e[x] = run;
+      const int r = st_lo + wid;
+      const int raw = num_ranges[r];
+      int32_t st = 0, ln = 0;
+      if (lane < rstride) {
+        st = range_start[(int64_t)r * rstride + lane];
+        ln = range_len[(int64_t)r * rstride + lane];
       }
+      const int n = (raw >= 0 && raw <= rstride) ? raw : -1;
+      const int64_t end = warp_inclusive_scan<int64_t>(lane < n ? (int64_t)max(ln, 0) : 0);
+      s_end[wid][lane] = end;
+      s_beg[wid][lane] = st;
+      if (lane == 0) s_cnt[wid] = n;
     }
     __syncthreads();
+    // a row of more than kStageCap ranges does not fit: the whole CTA takes
+    // the general path (the same decision in every thread)
+    for (int j = 0; j < st_n; ++j)
+      if (s_cnt[j] > kStageCap) st_n = 0;
   }
 
   const int32_t T = a.bs.size;
@@ -558,35 +591,30 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
     // Every token of the tile belongs to request st_lo.  A resolved range
     // whose blocks all lie in [1, num_blocks) becomes a window of positions
     // [plo, phi) whose slot is p + delta: no division, no lookup.
-    int64_t plo = 0, phi = 0, delta = 0;
+    PosWindow pw;
     RangeWindow win;
+    int64_t* out = a.slot_mapping + base;
+    if (t_lo + kTile <= a.num_tokens) {
+      // a full tile: every token is valid and below max_num_tokens
 #pragma unroll 1
-    for (int k = 0; k < kTokPerThread; ++k) {
-      const int32_t t = base + k * kThreads;
-      if (t >= a.max_num_tokens) break;
-      int64_t slot = kPad;
-      if (t < a.num_tokens) {
+      for (int k = 0; k < kTokPerThread; ++k, out += kThreads) {
         const int64_t pk = s_pos[k][threadIdx.x];
-        if (pk >= plo && pk < phi) {
-          slot = pk + delta;
-        } else if (pk < 0) {
-          err |= KV_ERR_BAD_POSITION;
-        } else {
-          int64_t lb, off;
-          a.bs.divmod(pk, lb, off);
-          if (win.has(st_lo, lb) || staged_find(s_end, s_beg, s_cnt, rstride, 0, st_lo, lb, win)) {
-            slot = slot_of(win.start + (lb - win.lo), off, T, a.num_blocks, err);
-            // block_size < 2^31, so ends below 2^32 keep hi * T inside int64
-            if (win.start >= 1 && win.start + (win.hi - win.lo) <= a.num_blocks &&
-                win.hi <= (INT64_MAX >> 31)) {
-              plo = win.lo * T;
-              phi = win.hi * T;
-              delta = (win.start - win.lo) * T;
-            }
-          }
-        }
+        *out = pw.has(pk) ? pk + pw.delta
+                          : window_miss(pk, a, s_end, s_beg, s_cnt, st_lo, win, pw, err);
       }
-      a.slot_mapping[t] = slot;
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < kTokPerThread; ++k, out += kThreads) {
+        const int32_t t = base + k * kThreads;
+        if (t >= a.max_num_tokens) break;
+        int64_t slot = kPad;
+        if (t < a.num_tokens) {
+          const int64_t pk = s_pos[k][threadIdx.x];
+          slot = pw.has(pk) ? pk + pw.delta
+                            : window_miss(pk, a, s_end, s_beg, s_cnt, st_lo, win, pw, err);
+        }
+        *out = slot;
+      }
     }
   } else {
     RangeWindow win;  // this thread's last resolved range
@@ -607,14 +635,12 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
           bool found = win.has(r, lb);
           const int j = r - st_lo;
           if (!found && j >= 0 && j < st_n) {
-            found = staged_find(s_end, s_beg, s_cnt, rstride, j, r, lb, win);
+            found = staged_find(s_end, s_beg, s_cnt, j, r, lb, win);
           } else if (!found) {
             const int32_t* rs = range_start + (int64_t)r * rstride;
             const int32_t* rl = range_len + (int64_t)r * rstride;
-            int32_t pre_s[kLanePrefetch], pre_l[kLanePrefetch];
-            lane_prefetch(rs, rl, rstride, vec4, pre_s, pre_l);
             const int nr = num_ranges[r];
-            if (nr >= 0 && nr <= rstride) found = range_walk(rs, rl, nr, pre_s, pre_l, r, lb, win);
+            if (nr >= 0 && nr <= rstride) found = range_walk_plain(rs, rl, nr, r, lb, win);
           }
           if (found) slot = slot_of(win.start + (lb - win.lo), off, T, a.num_blocks, err);
         }
@@ -760,10 +786,10 @@ extern "C" int kv_slot_mapping_range(const int32_t* query_start_loc, const int64
   const int64_t tile = (int64_t)kThreads * tpt;
   if (tpt > 1 && range_stride > 0 && num_reqs > 0 &&
       (int64_t)num_tokens * kStageReqs * 2 >= tile * num_reqs) {
-    // staged range ends and starts, then query_start_loc
-    const size_t smem =
-        (size_t)kStageReqs * range_stride * (sizeof(int64_t) + sizeof(int32_t)) + qsl_smem;
-    const size_t static_smem = sizeof(int64_t) * tpt * kThreads + sizeof(int32_t) * kStageReqs;
+    const size_t smem = qsl_smem;
+    const size_t static_smem = sizeof(int64_t) * tpt * kThreads +
+                               (sizeof(int64_t) + sizeof(int32_t)) * kStageReqs * kStageCap +
+                               sizeof(int32_t) * kStageReqs;
     auto kernel = tpt == 4 ? slot_mapping_range_staged_kernel<4>
                            : slot_mapping_range_staged_kernel<8>;
     if (smem + static_smem > 48 * 1024 &&

@@ -209,11 +209,14 @@ def test_range_equals_paged_with_256_ranges(seed, pad):
 # Tiles of 256, 1024 and 2048 tokens (one, four and eight tokens per thread)
 # whose tokens belong to exactly 8 requests (descriptors staged per CTA) or
 # to 9 (each lane walks its own request's ranges); some rows malformed.
+# Rows of up to 40 ranges: those of more than 32 cannot be staged and their
+# tiles take the general path.
+@pytest.mark.parametrize("S", [12, 40])
 @pytest.mark.parametrize("per_req,pad", [(32, 0), (31, 0), (128, 400_000), (127, 400_000),
                                          (256, 800_000), (255, 800_000)])
-def test_range_staging_boundary(per_req, pad):
-    rng = np.random.default_rng(3500 + per_req)
-    T, R, S = 16, 40, 12
+def test_range_staging_boundary(per_req, pad, S):
+    rng = np.random.default_rng(3500 + per_req + S)
+    T, R = 16, 40
     q = (np.arange(R + 1) * per_req).astype(np.int32)
     N = int(q[-1])
     rs = rng.integers(1, 5000, size=(R, S)).astype(np.int32)
