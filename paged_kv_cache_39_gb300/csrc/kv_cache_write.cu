@@ -15,7 +15,8 @@
 // takes 4 consecutive tokens of one layer (their slots in one load, one lane
 // each), so a warp writes the consecutive rows a prefill places in one block
 // back to back (measured +5 % over one row per step); a small batch keeps one
-// row per warp so its latency is one row's.
+// row per warp so its latency is one row's, and requests the row before the
+// slot so that the slot and row loads share one round trip.
 // Warps walk these groups in a grid-stride loop over a persistent grid sized
 // to the SM count.  Everything is 64-bit addressed: a 32-layer cache passes
 // 2^32 bytes.
@@ -29,10 +30,23 @@ constexpr int kVecPerLane = 4;                 // 16-byte vectors per lane per c
 constexpr int kChunkVecs = 32 * kVecPerLane;   // 2 KiB per K (and V) chunk
 
 
+// The token's slot, read by every lane (one broadcast); issued in program
+// order after the loads before it.
+__device__ __forceinline__ int64_t ld_slot(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.global.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
 // Move one (layer, token) row pair to its slot (nothing for PAD or errors).
+// With kLoadSlot the slot is read from *sp only once the row's first chunk
+// has been requested: the K and V rows do not depend on the slot, so the two
+// round trips overlap (a decode batch's write is one round trip, not two).
+template <bool kLoadSlot>
 __device__ __forceinline__ void write_row(const uint4* __restrict__ ks,
                                           const uint4* __restrict__ vs, int64_t s,
-                                          int64_t layer, uint4* __restrict__ k_cache,
+                                          const int64_t* sp, int64_t layer,
+                                          uint4* __restrict__ k_cache,
                                           uint4* __restrict__ v_cache, int64_t num_blocks,
                                           int32_t block_size, int32_t row_vecs, int lane,
                                           uint32_t& err) {
@@ -46,6 +60,7 @@ __device__ __forceinline__ void write_row(const uint4* __restrict__ ks,
         vr[j] = ld_stream(vs + v);
       }
     }
+    if (kLoadSlot && c0 == 0) s = ld_slot(sp);
     if (s < 0) return;  // PAD: nothing to store (warp-uniform)
     const int64_t b = s / block_size;
     if (b == kNull) { err |= KV_ERR_NULL_WRITE; return; }
@@ -82,14 +97,20 @@ cache_write_kernel(const uint4* __restrict__ key, const uint4* __restrict__ valu
   for (int64_t u = warp0; u < units; u += nwarps) {
     const int64_t layer = u / groups;
     const int64_t t0 = (u - layer * groups) * kRowsPerWarp;
+    if constexpr (kRowsPerWarp == 1) {
+      const int64_t i = layer * num_tokens + t0;
+      write_row<true>(key + i * row_vecs, value + i * row_vecs, 0, slot_mapping + t0, layer,
+                      k_cache, v_cache, num_blocks, block_size, row_vecs, lane, err);
+      continue;
+    }
     const int nt = (int)(num_tokens - t0 < kRowsPerWarp ? num_tokens - t0 : kRowsPerWarp);
     // the slots of the group, one lane each, then shared by the warp
     const int64_t my_s = lane < nt ? slot_mapping[t0 + lane] : -1;
     for (int k = 0; k < nt; ++k) {
       const int64_t s = __shfl_sync(kFull, my_s, k);
       const int64_t i = layer * num_tokens + t0 + k;
-      write_row(key + i * row_vecs, value + i * row_vecs, s, layer, k_cache, v_cache,
-                num_blocks, block_size, row_vecs, lane, err);
+      write_row<false>(key + i * row_vecs, value + i * row_vecs, s, nullptr, layer, k_cache,
+                       v_cache, num_blocks, block_size, row_vecs, lane, err);
     }
   }
   report(err_word, err);
