@@ -168,3 +168,64 @@ def test_gathers_and_copies_stress(seed):
         kv.kv_copy_blocks(kd2, vd2, cuda(sb), cuda(db), err=e, bulk=bulk)
         assert int(e.item()) == exp_ce
         assert np.array_equal(bits(kd2), ek) and np.array_equal(bits(vd2), ev)
+
+
+def _prefill_batch(rng):
+    """A large prefill-like batch (170k-700k tokens over at most 12 requests):
+    the size at which the range map stages each tile's descriptors in shared
+    memory.  Positions mostly run on from a random start, with jumps,
+    negative and out-of-range values; descriptor rows are adversarial: empty,
+    negative and zero lengths, null starts, starts whose ranges run past the
+    pool, counts above the stride, rows of more than 32 ranges."""
+    R = int(rng.integers(1, 13))
+    N = int(rng.integers(170_000, 700_000))
+    cuts = np.sort(rng.integers(0, N + 1, size=R - 1))
+    lens = np.diff(np.concatenate([[0], cuts, [N]]))
+    shift = int(rng.choice([0, 0, 7]))
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64) + shift
+    q[-1] = min(q[-1], N)
+    n_max = N + int(rng.choice([0, 5, 3000]))
+    T = int(rng.choice([16, 16, 32]))
+    B = 400_000
+    pos = np.empty(N, np.int64)
+    for r in range(R):
+        lo, hi = int(q[r]), int(q[r + 1])
+        pos[lo:hi] = int(rng.integers(0, 20_000)) + np.arange(hi - lo)
+    pos[:q[0]] = rng.integers(0, 1000, size=int(q[0]))
+    jumps = rng.integers(0, N, size=int(rng.integers(0, 50)))
+    pos[jumps] = rng.integers(-3, 2_000_000, size=len(jumps))
+    S = int(rng.choice([8, 32, 40, 256]))
+    rs = rng.integers(1, B - 3000, size=(R, S)).astype(np.int32)
+    rl = rng.integers(1, 3000, size=(R, S)).astype(np.int32)
+    nr = rng.integers(0, min(S, 40) + 1, size=R).astype(np.int32)
+    mask = rng.random((R, S))
+    rl[mask < 0.03] = 0
+    rl[(mask >= 0.03) & (mask < 0.05)] = -1
+    rs[(mask >= 0.05) & (mask < 0.08)] = 0
+    rs[(mask >= 0.08) & (mask < 0.11)] = B - 10
+    rs[(mask >= 0.11) & (mask < 0.12)] = -5
+    if R > 1 and rng.random() < 0.3:
+        nr[rng.integers(0, R)] = S + 1
+    return T, R, q.astype(np.int32), N, n_max, B, pos, rs, rl, nr
+
+
+@pytest.mark.parametrize("seed", range(max(1, len(SEEDS) // 4)))
+def test_range_staged_stress(seed):
+    rng = np.random.default_rng(90_000 + seed)
+    T, R, q, N, n_max, B, pos, rs, rl, nr = _prefill_batch(rng)
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    e = err_word()
+    s = kv.kv_slot_mapping_range(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B,
+                                 max_num_tokens=n_max, err=e)
+    assert int(e.item()) == exp_e
+    got = s.cpu().numpy()
+    assert np.array_equal(got, exp_s), f"first difference at token {int(np.argmax(got != exp_s))}"
+    # the paged map over the same blocks agrees wherever the table holds them
+    if (nr >= 0).all() and (nr <= rs.shape[1]).all() and (rl[:, :] > 0).all():
+        stride = wl.table_stride_for(int(np.maximum(rl, 0).sum(axis=1).max()) + 1, T)
+        table = oracle.table_from_ranges(rs, rl, nr, stride)
+        ep, _ = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
+        e2 = err_word()
+        sp = kv.kv_slot_mapping_paged(cuda(q), cuda(pos), cuda(table), T, B,
+                                      max_num_tokens=n_max, err=e2)
+        assert np.array_equal(sp.cpu().numpy(), ep)
