@@ -1260,10 +1260,12 @@ def main():
                 "alg_bytes_per_launch": int(dom.alg_bytes),
                 "avg_launch_us": round(dom_avg_ms * 1e3, 2),
                 "launch_floor_us": floor_us,
+                "frac_of_launch_floor": round(floor_us / (dom_avg_ms * 1e3), 4),
                 "regime": "latency: 256 tokens move a few KB to 2 MB per kernel, so every "
                           "kernel of the step is a chain of dependent DRAM round trips on top "
                           "of the launch; launch_floor_us is one replay of a graph holding a "
-                          "single one-element kernel",
+                          "single one-element kernel, timed the same way, and "
+                          "frac_of_launch_floor that floor over this kernel's time",
                 "timing": f"each call alone, L2 flushed before it, mean of {reps} launches"}
     same_run_copy = copy_ceiling(torch, dev, flush_buf, reps=5)["torch_copy_GBps_median"]
 
