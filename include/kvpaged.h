@@ -177,8 +177,10 @@ int kv_slot_mapping_paged_cp(const int32_t* query_start_loc, const int64_t* posi
  *
  * Defined by [RNG] The Innovation: physical_block = range_start +
  * (pos // block_size - range_cum); positions outside every range get the
- * same PAD id as the paged call.  The descriptor rows are loaded once per
- * warp of 32 consecutive tokens of one request, never per position.
+ * same PAD id as the paged call.  Descriptors are never loaded per position:
+ * a lane reuses the range it resolved last, a warp of tokens of one request
+ * reads 32 descriptors at once, and on large prefill batches a CTA stages
+ * its tile's requests' first 32 descriptors in shared memory once.
  *
  *   range_start, range_len  int32 [num_reqs, range_stride]; request r's ranges
  *                           i < num_ranges[r] in logical order: range i holds
