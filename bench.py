@@ -1058,11 +1058,15 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     three prepared calls, and copies both slot mappings and the error word
     back to pinned host memory, where the host checks them.
 
-    Measured the way a serving loop runs it: each of two buffer sets holds the
-    whole step (upload, the error word reset, the three calls, read-back)
-    captured once in a CUDA graph; step k+1's graph is launched before the
-    host consumes step k's read-back; value = steps / wall time.  The same
-    step alone, waited for, is reported as `sync_ms_per_step`."""
+    Measured the way a pipelined serving loop runs it, inputs prepared one
+    step ahead and results checked two steps behind: three buffer sets, and
+    for set j a CUDA graph that runs step j on it while two forked branches
+    upload step j+1's inputs into the next set and read step j-1's outputs
+    back from the previous one.  One graph launch per step, each moving one
+    step's inputs up and one step's outputs down; after launching step j the
+    host waits for step j-1 and checks the error word and a slot of step j-2;
+    value = steps / wall time.  The same step run serially (upload, calls,
+    read-back) and waited for is reported as `sync_ms_per_step`."""
     k = built.keep
     w, lay = k["w"], k["lay"]
     dev = k["qsl"].device
@@ -1088,14 +1092,13 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     exp_r = k["slot_r"].cpu().numpy()
     probe = int(np.argmax(exp_p >= 0))
 
-    class Slot:
-        """One set of device buffers and the step's graph."""
+    class Set:
+        """One set of device buffers, its read-back buffer and prepared calls."""
 
         def __init__(self):
             self.d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
             d = {n: self.d_stage[offs[n]:offs[n] + k[n].numel() * k[n].element_size()]
                  .view(k[n].dtype).view(k[n].shape) for n in names}
-            # outputs: both slot mappings and the error word, read back with one copy
             self.d_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
             self.h_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
             h = self.h_out.numpy()
@@ -1104,82 +1107,126 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
             self.h_err = h[2 * n_slot * 8:2 * n_slot * 8 + 4].view(np.int32)
             slot_p = self.d_out[:n_slot * 8].view(torch.int64)
             slot_r = self.d_out[n_slot * 8:2 * n_slot * 8].view(torch.int64)
-            err = self.d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)
-            # validated once; the graph replays them with the cached pointers
-            calls = [
+            self.err = self.d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)
+            # validated once; the graphs replay them with the cached pointers
+            self.calls = [
                 kv.kv_slot_mapping_paged(d["qsl"], d["pos"], d["table"], T, B,
-                                         max_num_tokens=n_max, slot_mapping=slot_p, err=err,
-                                         prepare=True),
+                                         max_num_tokens=n_max, slot_mapping=slot_p,
+                                         err=self.err, prepare=True),
                 kv.kv_slot_mapping_range(d["qsl"], d["pos"], d["rs"], d["rl"], d["nr"], T, B,
-                                         max_num_tokens=n_max, slot_mapping=slot_r, err=err,
-                                         prepare=True),
-                kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=err,
+                                         max_num_tokens=n_max, slot_mapping=slot_r,
+                                         err=self.err, prepare=True),
+                kv.kv_cache_write(d["key"], d["val"], k["kc"], k["vc"], slot_p, err=self.err,
                                   prepare=True),
             ]
-
-            def whole_step():
-                self.d_stage.copy_(h_stage, non_blocking=True)
-                err.zero_()
-                for c in calls:
-                    c()
-                self.h_out.copy_(self.d_out, non_blocking=True)
-
-            self.graph = GraphStep(torch, [whole_step])
             self.done = torch.cuda.Event()
 
-        def launch(self):
-            self.graph.replay()
-            self.done.record()
+        def upload(self):
+            self.d_stage.copy_(h_stage, non_blocking=True)
 
-        def consume(self):
-            self.done.synchronize()
+        def compute(self):
+            self.err.zero_()
+            for c in self.calls:
+                c()
+
+        def download(self):
+            self.h_out.copy_(self.d_out, non_blocking=True)
+
+        def check(self):
             if int(self.h_err[0]) != 0:
                 raise RuntimeError("end-to-end step reported data errors")
             if int(self.h_slot_p[probe]) != int(exp_p[probe]):
                 raise RuntimeError("end-to-end step read back a wrong slot")
 
-    slots = [Slot(), Slot()]
+    sets = [Set(), Set(), Set()]
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
+
+    def pipelined(j):
+        """Step j on set j; step j+1's inputs up into set j+1, step j-1's
+        outputs back from set j-1 (sets modulo 3), on two side branches."""
+        cur = torch.cuda.current_stream()
+        up_stream.wait_stream(cur)
+        down_stream.wait_stream(cur)
+        with torch.cuda.stream(up_stream):
+            sets[(j + 1) % 3].upload()
+        with torch.cuda.stream(down_stream):
+            sets[(j + 2) % 3].download()
+        sets[j % 3].compute()
+        cur.wait_stream(up_stream)
+        cur.wait_stream(down_stream)
+
+    def capture(fn):
+        for st in sets:
+            st.upload()
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    graphs = [capture(lambda j=j: pipelined(j)) for j in range(3)]
+    serial = capture(lambda: (sets[0].upload(), sets[0].compute(), sets[0].download()))
+    step_no = [0]
 
     def run(n):
-        for s in range(n):
-            slots[s % 2].launch()
-            if s > 0:
-                slots[(s - 1) % 2].consume()
-        slots[(n - 1) % 2].consume()
+        """n more steps; returns after all of them have been checked."""
+        first = step_no[0]
+        for j in range(first, first + n + 2):  # two more launches read the last steps back
+            graphs[j % 3].replay()
+            sets[j % 3].done.record()
+            if j > first:
+                sets[(j - 1) % 3].done.synchronize()
+                if j - 2 >= first:
+                    sets[(j - 2) % 3].check()
+        step_no[0] = first + n + 2
 
-    run(4)  # warm-up
+    for st in sets:
+        st.upload()
+    run(6)  # warm-up
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     run(steps)
     wall = time.perf_counter() - t0
+    n_steps = steps + 2  # the two extra launches each did a whole step's work too
 
-    # every step on its own: the graph launched and waited for (L2 flushed before)
+    # every step on its own, serially: upload, calls, read-back, waited for
+    # (L2 flushed before)
     times = []
     for s in range(min(steps, 200)):
         flush_l2(flush_buf)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
-        slots[0].launch()
-        slots[0].consume()
+        serial.replay()
+        sets[0].done.record()
+        sets[0].done.synchronize()
+        sets[0].check()
         times.append(time.perf_counter() - t1)
     # what came back is the device path's answer on the same inputs
-    for sl in slots:
-        if (int(sl.h_err[0]) != 0 or not np.array_equal(sl.h_slot_p, exp_p)
-                or not np.array_equal(sl.h_slot_r, exp_r)):
+    for st in sets:
+        if (int(st.h_err[0]) != 0 or not np.array_equal(st.h_slot_p, exp_p)
+                or not np.array_equal(st.h_slot_r, exp_r)):
             raise RuntimeError("end-to-end read-back differs from the device-resident step")
-    ms = wall / steps * 1e3
-    del slots
+    ms = wall / n_steps * 1e3
+    del graphs, serial, sets
     return {"value": round(built.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(out_bytes),
-            "ms_per_step": round(ms, 4), "steps": steps,
+            "ms_per_step": round(ms, 4), "steps": n_steps,
             "sync_ms_per_step": round(statistics.median(times) * 1e3, 4),
-            "note": "wall time over all steps: each step copies its packed inputs (positions, "
-                    "query_start_loc, block table, range descriptors, new K/V rows) from pinned "
-                    "host memory, runs the three prepared calls and copies both slot mappings "
-                    "and the error word back to pinned host memory, all captured in one CUDA "
-                    "graph per buffer set (two sets); the host launches step k+1 before checking "
-                    "step k's error word and a slot; sync_ms_per_step: median of the same step "
-                    "launched alone and waited for, L2 flushed before it"}
+            "note": "wall time over all steps: each step copies one step's packed inputs "
+                    "(positions, query_start_loc, block table, range descriptors, new K/V "
+                    "rows) from pinned host memory and reads one step's slot mappings and "
+                    "error word back to pinned host memory; three buffer sets, each with a "
+                    "CUDA graph that runs its step while forked branches upload the next "
+                    "step's inputs and read the previous step's outputs back; the host checks "
+                    "every step's error word and a slot two steps behind; steps run back to "
+                    "back with no L2 flush (each step's inputs arrive fresh by its upload, "
+                    "through L2), so a step can be a little faster than the flushed "
+                    "device-resident one; sync_ms_per_step: median of one step run serially "
+                    "(upload, calls, read-back) and waited for, L2 flushed before it"}
 
 
 # --------------------------------------------------------------------------
