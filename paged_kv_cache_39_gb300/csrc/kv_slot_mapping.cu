@@ -392,55 +392,27 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
 // ---------------------------------------------------------------------------
 // Range variant for large prefill batches and long contexts (4 or 8 tokens
 // per thread, requests long enough to fill a tile).  A CTA whose token tile
-// belongs to at most kStageReqs requests stages those requests' descriptors
-// in shared memory once: one load per descriptor for the whole CTA, a warp
-// per request turns the lengths into range ends (logical block ranges
-// [end_{i-1}, end_i)), and a barrier publishes them.  Each token then
-// resolves its block from shared memory: a binary search for the first end
-// past its logical block, skipped while the token stays inside the range the
-// thread resolved last -- the descriptor once per position block, arithmetic
-// per position.  Other tiles let each lane walk its own request's ranges.
-// The grid-wide sweep over every descriptor row sets BAD_RANGE as in the
-// kernel above.
+// belongs to at most kStageReqs requests stages, for each of them, the count
+// and the first kStageCap descriptors in shared memory: one warp per request,
+// one load per descriptor, one warp scan turning the lengths into range ends
+// (logical block ranges [end_{i-1}, end_i)).  A token resolves its block from
+// there by a binary search for the first end past its logical block; when the
+// whole tile lies in one request, a range whose blocks are all valid becomes
+// a window of positions whose slot is the position plus a constant, so a
+// token inside the range its thread resolved last costs one addition -- the
+// descriptor once per position block, arithmetic per position.  Tiles of more
+// requests, or a request of more than kStageCap ranges, let each thread walk
+// its own request's ranges.  The grid-wide sweep over every descriptor row
+// sets BAD_RANGE as in the kernel above.
 
 constexpr int kStageReqs = 8;  // requests a CTA stages (one warp each)
 constexpr int kStageCap = 32;  // descriptors staged per request (one per lane)
 static_assert(kStageReqs == kThreads / 32, "one warp stages each request");
 
 // Logical block lb of request r by a walk of its descriptor row in global
-// memory (pre_*: its first kLanePrefetch descriptors, nr: its count).
-// Sets win on success.
+// memory (nr: its count), for tiles that could not be staged.  Sets win on
+// success.
 __device__ __forceinline__ bool range_walk(const int32_t* __restrict__ rs,
-                                           const int32_t* __restrict__ rl, int nr,
-                                           const int32_t (&pre_s)[kLanePrefetch],
-                                           const int32_t (&pre_l)[kLanePrefetch], int r,
-                                           int64_t lb, RangeWindow& win) {
-  int64_t cum = 0;
-#pragma unroll
-  for (int i = 0; i < kLanePrefetch; ++i) {
-    if (i < nr) {
-      const int64_t len = max(pre_l[i], 0);
-      if (lb < cum + len) {
-        win = RangeWindow{r, cum, cum + len, pre_s[i]};
-        return true;
-      }
-      cum += len;
-    }
-  }
-  for (int i = kLanePrefetch; i < nr; ++i) {
-    const int64_t len = max(rl[i], 0);
-    if (lb < cum + len) {
-      win = RangeWindow{r, cum, cum + len, rs[i]};
-      return true;
-    }
-    cum += len;
-  }
-  return false;
-}
-
-// The same walk without the prefetched head (fewer registers, for tiles
-// that could not be staged).
-__device__ __forceinline__ bool range_walk_plain(const int32_t* __restrict__ rs,
                                                  const int32_t* __restrict__ rl, int nr, int r,
                                                  int64_t lb, RangeWindow& win) {
   int64_t cum = 0;
@@ -640,7 +612,7 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
             const int32_t* rs = range_start + (int64_t)r * rstride;
             const int32_t* rl = range_len + (int64_t)r * rstride;
             const int nr = num_ranges[r];
-            if (nr >= 0 && nr <= rstride) found = range_walk_plain(rs, rl, nr, r, lb, win);
+            if (nr >= 0 && nr <= rstride) found = range_walk(rs, rl, nr, r, lb, win);
           }
           if (found) slot = slot_of(win.start + (lb - win.lo), off, T, a.num_blocks, err);
         }
