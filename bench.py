@@ -1336,6 +1336,7 @@ def main():
     gather = gather_long(torch, kv, wl, dev, max(args.detail_reps, 5), flush_buf, stream,
                          (peak, peak_kind), same_run_copy, small=args.small)
     line["gather_GBps"] = gather["GBps"]
+    line["gather_roofline"] = gather["roofline"]  # the metric's second half
     line["gather"] = gather
     line["decode_step_with_gather"] = decode_step_with_gather(
         torch, built, min(args.steps, 500), flush_buf, stream, (peak, peak_kind), args)
