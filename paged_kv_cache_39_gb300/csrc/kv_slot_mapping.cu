@@ -477,9 +477,9 @@ __device__ __forceinline__ int64_t window_miss(int64_t p, const SlotArgs& a,
   return slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err);
 }
 
-// At most 64 registers: four CTAs per SM keep the grid within one wave
-// (512 CTAs for 1M positions at 8 tokens per thread); 80 registers left
-// three per SM and a second wave.
+// At most 64 registers (it needs 56): four CTAs per SM keep the grid within
+// one wave (512 CTAs for 1M positions at 8 tokens per thread); an earlier
+// form at 80 registers ran three per SM and needed a second wave.
 template <int kTokPerThread>
 __global__ void __launch_bounds__(kThreads, 4)
 slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
