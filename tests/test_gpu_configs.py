@@ -127,7 +127,8 @@ def test_mixed_gather_layers():
     puts byte offsets far past 2^32: the table gather, its bulk-copy form and
     the range-addressed gather, every row against the oracle's source rows.
     The batch is written first, so the gathered spans also hold the new
-    tokens' rows (gather after write returns what was written)."""
+    tokens' rows (gather after write returns what was written).  Then the
+    copy-on-write kernels on the same caches, every layer."""
     w = mixed_workload()
     lay = w.layouts["G"]
     T, B, L, H, D, E = (w.block_size, w.num_blocks, w.num_layers, w.num_kv_heads, w.head_dim,
@@ -179,6 +180,28 @@ def test_mixed_gather_layers():
         sample_host_check(outs["table"][0], lambda n: kflat[n].cpu().numpy().view(np.uint16),
                           src, E, sample)
         del outs
+    # copy-on-write on the same caches: 1024 forks by the vector kernel and
+    # 1024 by the bulk-copy kernel, disjoint blocks, every layer (offsets past
+    # 2^32 bytes); each destination block of every layer must equal its
+    # source's earlier contents, and untouched blocks keep theirs
+    perm = rng.permutation(np.arange(1, B, dtype=np.int32))
+    untouched = torch.from_numpy(perm[4096:4096 + 64].astype(np.int64)).to(dev())
+    k_keep, v_keep = kc[:, untouched].clone(), vc[:, untouched].clone()
+    for n, bulk in ((0, False), (1, True)):
+        src_b = perm[2048 * n:2048 * n + 1024]
+        dst_b = perm[2048 * n + 1024:2048 * n + 2048]
+        s_idx = torch.from_numpy(src_b.astype(np.int64)).to(dev())
+        d_idx = torch.from_numpy(dst_b.astype(np.int64)).to(dev())
+        k_src, v_src = kc[:, s_idx].clone(), vc[:, s_idx].clone()
+        e = err_word()
+        kv.kv_copy_blocks(kc, vc, cuda(src_b), cuda(dst_b), err=e, bulk=bulk)
+        assert int(e.item()) == 0
+        assert torch.equal(kc[:, d_idx].view(torch.int16), k_src.view(torch.int16)), bulk
+        assert torch.equal(vc[:, d_idx].view(torch.int16), v_src.view(torch.int16)), bulk
+        assert torch.equal(kc[:, s_idx].view(torch.int16), k_src.view(torch.int16))
+        del k_src, v_src
+    assert torch.equal(kc[:, untouched].view(torch.int16), k_keep.view(torch.int16))
+    assert torch.equal(vc[:, untouched].view(torch.int16), v_keep.view(torch.int16))
 
 
 @pytest.mark.parametrize("layout", ["P", "G"])
