@@ -432,6 +432,28 @@ def test_cp_slot_mapping_parity_and_partition(W, I, T):
     assert np.array_equal(owned, (ref >= 0).astype(np.int64))
 
 
+@pytest.mark.parametrize("W,I", [(2, 1), (4, 16)])
+def test_cp_slot_mapping_long_context(W, I):
+    """The context-parallel map at the long-context size (1M positions, four
+    tokens per thread), every rank, through the permuted table."""
+    w = wl.long_context()
+    table = w.layouts["P"].table
+    T, B, N = w.block_size, w.num_blocks, w.num_tokens
+    owned = np.zeros(N, np.int64)
+    q, pos, tab = cuda(w.qsl), cuda(w.positions), cuda(table)
+    for k in range(W):
+        exp_s, exp_e = oracle.slot_mapping_paged_cp(w.qsl, w.positions, table, N, N, T, B, W,
+                                                    k, I)
+        e = err_word()
+        s = kv.kv_slot_mapping_paged_cp(q, pos, tab, T, B, W, k, I, err=e)
+        got = s.cpu().numpy()
+        assert int(e.item()) == exp_e
+        assert np.array_equal(got, exp_s)
+        owned += got >= 0
+    # every token of the (fully owned) contexts lives on exactly one rank
+    assert (owned == 1).all()
+
+
 @pytest.mark.parametrize("bulk", [False, True])
 @pytest.mark.parametrize("T,H,D,R", [(16, 32, 128, 7), (32, 8, 128, 9), (16, 8, 128, 2048),
                                      (16, 8, 128, 2049), (4, 20, 1024, 5), (16, 1, 8, 33)])
