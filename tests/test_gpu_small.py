@@ -576,6 +576,61 @@ def test_slot_mapping_with_slots_past_int32(T):
     assert int(e_.item()) == exp_ce and np.array_equal(sc.cpu().numpy(), exp_c)
 
 
+@pytest.mark.parametrize("R,lo,hi,pad", [(5000, 20, 100, 0), (3000, 40, 160, 700_000),
+                                         (12000, 1, 60, 0)])
+def test_range_many_short_requests_past_one_wave(R, lo, hi, pad):
+    """Batches beyond one wave of one token per thread made of many short
+    requests (decode-like chunks): the range map that walks each request's
+    ranges per lane, at four and eight tokens per thread, and the paged map
+    through the expanded table."""
+    rng = np.random.default_rng(17000 + R + pad)
+    T, S = 16, 8
+    lens = rng.integers(lo, hi, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    nr = rng.integers(1, S + 1, size=R).astype(np.int32)
+    rl = rng.integers(1, 5, size=(R, S)).astype(np.int32)
+    rs = np.zeros((R, S), np.int32)
+    cursor = 1
+    for r in range(R):
+        for i in range(S):
+            rs[r, i] = cursor
+            cursor += int(rl[r, i]) + int(rng.integers(0, 3))
+    B = cursor + 1
+    rl[rng.random((R, S)) < 0.01] = 0      # a few empty ranges
+    nr[rng.integers(0, R, size=3)] = S + 1  # a few malformed rows
+    pos = np.concatenate([rng.integers(0, 40 * T, size=int(n)) for n in lens]).astype(np.int64)
+    pos[rng.integers(0, N, size=5)] = -1
+    n_max = N + pad
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    s, e = run_range(q, pos, rs, rl, nr, N, n_max, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    stride = wl.table_stride_for(int(rl.sum(axis=1).max()), T)
+    table = oracle.table_from_ranges(rs, rl, np.minimum(nr, S), stride)
+    exp_p, exp_pe = oracle.slot_mapping_paged(q, pos, table, N, n_max, T, B)
+    sp, ep = run_paged(q, pos, table, N, n_max, T, B)
+    assert ep == exp_pe and np.array_equal(sp, exp_p)
+
+
+@pytest.mark.parametrize("T", [16, 24])
+def test_paged_wide_slots_four_tokens_per_thread(T):
+    """Slots past 2^31 on a batch beyond one wave (the paged map's 64-bit
+    form at four tokens per thread)."""
+    rng = np.random.default_rng(18000 + T)
+    B = 1 << 28
+    R, stride = 40, 128
+    table = rng.integers(0, B, size=(R, stride)).astype(np.int32)
+    table[rng.random(table.shape) < 0.05] = 0
+    lens = rng.integers(8000, 12000, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    pos = rng.integers(-1, stride * T + 30, size=N).astype(np.int64)
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, N, N + 3, T, B)
+    assert exp_s.max() > (1 << 31) and N > 320_000
+    s, e = run_paged(q, pos, table, N, N + 3, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+
+
 @pytest.mark.parametrize("L,N", [(1, 40003), (3, 13333)])
 def test_write_grouped_path(L, N):
     """Batches of tens of thousands of rows take the four-rows-per-warp write;
