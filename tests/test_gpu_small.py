@@ -612,6 +612,28 @@ def test_range_many_short_requests_past_one_wave(R, lo, hi, pad):
     assert ep == exp_pe and np.array_equal(sp, exp_p)
 
 
+def test_range_staged_with_qsl_in_global_memory():
+    """More requests than query_start_loc entries fit in shared memory (9000)
+    on a batch large enough for the staged range map (2.2M tokens, eight per
+    thread): the tile's requests are found by searching global memory."""
+    rng = np.random.default_rng(19000)
+    T, R, S = 16, 9000, 6
+    lens = rng.integers(150, 350, size=R)
+    q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(q[-1])
+    nr = rng.integers(1, S + 1, size=R).astype(np.int32)
+    rl = rng.integers(1, 12, size=(R, S)).astype(np.int32)
+    rs = rng.integers(1, 2_000_000, size=(R, S)).astype(np.int32)
+    nr[rng.integers(0, R, size=4)] = S + 2
+    pos = np.concatenate([int(rng.integers(0, 200)) + np.arange(int(n)) for n in lens])
+    pos = pos.astype(np.int64)
+    B = 2_000_020
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N, T, B)
+    s, e = run_range(q, pos, rs, rl, nr, N, N, T, B)
+    assert N > 2_000_000 and e == exp_e
+    assert np.array_equal(s, exp_s)
+
+
 @pytest.mark.parametrize("T", [16, 24])
 def test_paged_wide_slots_four_tokens_per_thread(T):
     """Slots past 2^31 on a batch beyond one wave (the paged map's 64-bit
