@@ -634,6 +634,65 @@ def test_range_staged_with_qsl_in_global_memory():
     assert np.array_equal(s, exp_s)
 
 
+@pytest.mark.parametrize("pad", [0, 700_000])
+def test_range_lengths_past_int32(pad):
+    """Ranges of 2^27 and 2^30 blocks (cumulative block counts past 2^31, so
+    every scan of the lengths needs 64 bits): positions at the start of each
+    range and one deep inside a huge range (its block is past the pool),
+    through the range map (one token per thread, and the staged kernel on a
+    long prefill), the fused range write and the range-addressed gather."""
+    rng = np.random.default_rng(20000 + pad)
+    T, H, D, R = 16, 1, 8, 4
+    big = [(10, 5), (100, 1 << 27), (50, 3), (120, 1 << 30), (200, 1 << 30), (300, 7)]
+    S = len(big)
+    B = 400 * R  # request r's blocks lie in [400 r, 400 r + 400)
+    rs = np.array([[st + 400 * r for st, _ in big] for r in range(R)], np.int32)
+    rl = np.array([[ln for _, ln in big]] * R, np.int32)
+    nr = np.full(R, S, np.int32)
+    ends = np.cumsum([ln for _, ln in big])
+    starts = ends - np.array([ln for _, ln in big])
+    lbs = [int(starts[i]) + j for i in range(S) for j in range(6)]
+    lbs += [int(starts[1]) + 5000, int(ends[-1]) + 2]  # past the pool; past every range
+    pos1 = np.array([lb * T + int(rng.integers(0, T)) for lb in lbs], np.int64)
+    reps = 6000 if pad else 1  # a long prefill of the same positions: the staged kernel
+    q = np.concatenate([[0], np.cumsum([len(lbs) * reps] * R)]).astype(np.int32)
+    pos = np.tile(pos1, reps * R)
+    N = int(q[-1])
+    exp_s, exp_e = oracle.slot_mapping_range(q, pos, rs, rl, nr, N, N + pad, T, B)
+    s, e = run_range(q, pos, rs, rl, nr, N, N + pad, T, B)
+    assert e == exp_e and np.array_equal(s, exp_s)
+    assert exp_e == kv.ERR_BITS["BAD_BLOCK"] and (exp_s[:N] >= 0).sum() == 6 * S * R * reps
+    if pad:
+        return
+    assert len(np.unique(exp_s[exp_s >= 0])) == 6 * S * R  # the write below has no races
+    # fused range write on a small cache
+    key = wl.bf16_normal((1, N, H, D), 210)
+    kc = wl.bf16_normal((1, B, T, H, D), 211)
+    ek, ev = bits(kc).copy(), bits(kc).copy()
+    exp_we = oracle.cache_write(bits(key), bits(key), ek, ev, exp_s[:N], B, T)
+    kc_d, vc_d = kc.to(dev()), kc.clone().to(dev())
+    e2 = err_word()
+    sf = kv.kv_slot_mapping_range_write(cuda(q), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B,
+                                        key.to(dev()), key.to(dev()), kc_d, vc_d, err=e2)
+    assert int(e2.item()) == exp_e | exp_we
+    assert np.array_equal(sf.cpu().numpy(), exp_s[:N])
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+    # range-addressed gather: spans at the start of the 2^27-block range
+    # (rows), deep inside it (blocks past the pool: zero rows) and in range 0
+    g0 = np.array([int(starts[1]) * T, 2_000_000_000, 0, int(starts[1]) * T + 3], np.int32)
+    g1 = (g0 + np.array([40, 33, 90, 17])).astype(np.int32)
+    rows = int((g1.astype(np.int64) - g0).sum())
+    src, exp_ge = oracle.gather_rows_range(0, B, T, rs, rl, nr, g0, g1, rows)
+    e3 = err_word()
+    ko, vo = kv.kv_cache_gather_range(kc_d, vc_d, cuda(rs), cuda(rl), cuda(nr), cuda(g0),
+                                      cuda(g1), out_rows=rows, err=e3)
+    assert int(e3.item()) == exp_ge and exp_ge == kv.ERR_BITS["BAD_BLOCK"]
+    kd = bits(kc_d).reshape(-1, H * D)
+    exp_rows = np.where((src >= 0)[:, None], kd[np.maximum(src, 0)], 0)
+    assert (src >= 0).sum() == 40 + 90 + 17
+    assert np.array_equal(bits(ko).reshape(-1, H * D), exp_rows)
+
+
 @pytest.mark.parametrize("T", [16, 24])
 def test_paged_wide_slots_four_tokens_per_thread(T):
     """Slots past 2^31 on a batch beyond one wave (the paged map's 64-bit
