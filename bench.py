@@ -11,7 +11,9 @@ step is
   3. kv_cache_write          (the new tokens' K/V rows to their slots)
 
 captured once in a CUDA graph and replayed, as a serving loop runs its decode
-steps; `value` is new tokens per second over the whole job.  The L2 is
+steps.  The range map reads nothing the other two write (it fills its own slot
+buffer), so the graph runs it on a second branch beside the paged map -> write
+chain.  `value` is new tokens per second over the whole job.  The L2 is
 flushed (a 256 MiB write, then a 256 MiB read) between timed steps, outside
 the timed events.  Beside it, in the same JSON line:
 
@@ -52,7 +54,8 @@ METRIC = "KV write+slot-map tokens/s and gather GB/s (frac of ~8 TB/s), paged vs
 FLUSH_BYTES = 512 << 20  # two halves of 256 MiB, each twice the 129 MB L2
 DECODE_DESC = ("decode step: 256 requests x 1 new token, context U{512..4096}, block_size 16, "
                "40960-block pool, KV 8x128 bf16 (one layer), 1-4 contiguous ranges per request; "
-               "step = paged slot map + range slot map + KV write")
+               "step = paged slot map + range slot map + KV write (one CUDA graph: paged map -> "
+               "write, the range map on a second branch)")
 GATHER_DESC = ("long-context gather: 8 requests x 131072 tokens, block_size 16, KV 8x128 bf16, "
                "whole context of every request into packed K/V buffers (8.59 GB moved)")
 
@@ -235,8 +238,38 @@ def gather_bytes(rows, row_bytes, blocks, R):
 
 
 class Built:
-    def __init__(self, name, desc, launches, tokens, keep):
+    """A workload's launches in stream order.  `branch` lists the indices of
+    launches that read nothing the others write and write nothing they read:
+    a step's graph runs those on a second branch (see step_fn)."""
+
+    def __init__(self, name, desc, launches, tokens, keep, branch=()):
         self.name, self.desc, self.launches, self.tokens, self.keep = name, desc, launches, tokens, keep
+        self.branch = tuple(branch)
+
+
+def forked(torch, side, chain, branch):
+    """One function running `chain` in order on the current stream and
+    `branch` in order on `side`, forked from the current stream's state and
+    joined back into it; captured in a CUDA graph, the two lists become two
+    branches of the graph."""
+    def run():
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        for fn in chain:
+            fn()
+        with torch.cuda.stream(side):
+            for fn in branch:
+                fn()
+        cur.wait_stream(side)
+    return run
+
+
+def step_fn(torch, built, side, extra=()):
+    """The whole step of `built` (plus `extra` launches after its chain) as
+    one function: the independent launches on a second branch."""
+    chain = [l.fn for i, l in enumerate(built.launches) if i not in built.branch]
+    branch = [built.launches[i].fn for i in built.branch]
+    return forked(torch, side, chain + [l.fn for l in extra], branch)
 
 
 def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
@@ -317,7 +350,9 @@ def build_decode(torch, kv, wl, dev, seed=1, extras=False, small=False):
     keep = dict(w=w, lay=lay, qsl=qsl, pos=pos, table=table, rs=rs, rl=rl, nr=nr, g0=g0, g1=g1,
                 key=key, val=val, kc=kc, vc=vc, slot_p=slot_p, slot_r=slot_r, err=err,
                 k_out=k_out, v_out=v_out, rows=rows, gather=gather)
-    return Built("decode", DECODE_DESC, launches, N, keep)
+    # the range map (its own slot buffer) is independent of the paged map and
+    # the write, which reads the paged map's slots
+    return Built("decode", DECODE_DESC, launches, N, keep, branch=(1,))
 
 
 def build_mixed(torch, kv, wl, dev, small=False):
@@ -1033,7 +1068,9 @@ def decode_step_with_gather(torch, built, steps, flush_buf, stream, peak, args):
     avg_ms = sum(per[-1]) / len(per[-1])
     achieved = g.alg_bytes / (avg_ms * 1e-3) / 1e9
     ms = sum(step_ms) / len(step_ms)
-    g_ms = graph_replay_ms(torch, [l.fn for l in b.launches], steps, flush_buf)
+    side = torch.cuda.Stream(device=built.keep["qsl"].device)
+    g_ms = graph_replay_ms(torch, [step_fn(torch, built, side, extra=[b.launches[-1]])], steps,
+                           flush_buf)
     return {"ms_per_step": round(ms, 4), "tokens_per_s": round(b.tokens / (ms * 1e-3), 1),
             "graph_ms_per_step": round(g_ms, 4),
             "graph_tokens_per_s": round(b.tokens / (g_ms * 1e-3), 1),
@@ -1044,8 +1081,9 @@ def decode_step_with_gather(torch, built, steps, flush_buf, stream, peak, args):
                                 "traffic": profiled_traffic(g.kernel, "decode"),
                                 "alg_bytes_per_launch": int(g.alg_bytes),
                                 "avg_launch_us": round(avg_ms * 1e3, 2)},
-            "note": "per-launch events inside each step (L2 flushed between steps); graph: the "
-                    "four calls in one CUDA graph"}
+            "note": "per-launch events inside each step, in stream order (L2 flushed between "
+                    "steps); graph: the four calls in one CUDA graph, the range map on a second "
+                    "branch"}
 
 
 # --------------------------------------------------------------------------
@@ -1055,8 +1093,9 @@ def decode_step_with_gather(torch, built, steps, flush_buf, stream, peak, args):
 def e2e_step(torch, kv, built, steps, flush_buf, stream):
     """The headline step through the public API from host memory: every step
     copies its inputs from pinned host memory (packed, one copy), runs the
-    three prepared calls, and copies both slot mappings and the error word
-    back to pinned host memory, where the host checks them.
+    three prepared calls (paged map -> write, the range map on a second
+    branch, as in the device-resident step), and copies both slot mappings and
+    the error word back to pinned host memory, where the host checks them.
 
     Measured the way a pipelined serving loop runs it, inputs prepared one
     step ahead and results checked two steps behind: three buffer sets, and
@@ -1126,8 +1165,8 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
 
         def compute(self):
             self.err.zero_()
-            for c in self.calls:
-                c()
+            paged, rng, write = self.calls
+            forked(torch, range_stream, [paged, write], [rng])()
 
         def download(self):
             self.h_out.copy_(self.d_out, non_blocking=True)
@@ -1141,6 +1180,7 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     sets = [Set(), Set(), Set()]
     up_stream = torch.cuda.Stream(device=dev)
     down_stream = torch.cuda.Stream(device=dev)
+    range_stream = torch.cuda.Stream(device=dev)
 
     def pipelined(j):
         """Step j on set j; step j+1's inputs up into set j+1, step j-1's
@@ -1276,7 +1316,8 @@ def main():
     torch.cuda.synchronize()
     if int(built.keep["err"].item()) != 0:
         raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
-    step = GraphStep(torch, [l.fn for l in built.launches])
+    side = torch.cuda.Stream(device=dev)
+    step = GraphStep(torch, [step_fn(torch, built, side)])
 
     with ClockSampler() as clocks:
         kdist.barrier(dev)
@@ -1324,8 +1365,9 @@ def main():
             "config": {"workload": built.desc + (" [small]" if args.small else ""),
                        "l2": "flushed between timed steps outside the events (256 MiB written, then "
                              "another 256 MiB read)",
-                       "timing": "the step's three calls captured once in a CUDA graph, one "
-                                 "replay per step, CUDA events around each replay",
+                       "timing": "the step's three calls captured once in a CUDA graph (paged "
+                                 "map -> write; the range map on a second branch), one replay "
+                                 "per step, CUDA events around each replay",
                        "parallelism": "replicas" if rk.world_size > 1 else "single GPU",
                        "per_gpu_tokens_per_step": built.tokens},
             "kernels": kernels, "roofline": roofline,

@@ -145,6 +145,93 @@ def test_decode_step_captured_once_replayed_on_new_batches(bulk, mode, fused):
         assert int(err.item()) == (e1 | e2 | e3) == 0
 
 
+def _runs(table, R_pad, stride):
+    """Each request's table row as contiguous range descriptors (runs of
+    consecutive block ids), padded to `stride` descriptors per request."""
+    rs = np.zeros((R_pad, stride), np.int32)
+    rl = np.zeros((R_pad, stride), np.int32)
+    nr = np.zeros(R_pad, np.int32)
+    for r in range(R_pad):
+        row = table[r][table[r] != 0]
+        for b in row:
+            k = nr[r]
+            if k and rs[r, k - 1] + rl[r, k - 1] == b:
+                rl[r, k - 1] += 1
+            else:
+                rs[r, k], rl[r, k] = b, 1
+                nr[r] += 1
+    return rs, rl, nr
+
+
+def test_decode_step_with_the_range_map_on_a_second_graph_branch():
+    """The decode step as the benchmark captures it: paged map -> write on the
+    capturing stream and the range map, into its own slot buffer, on a forked
+    stream joined back before the capture ends (two branches of one graph,
+    both reporting into one error word).  Replayed on new batches, both slot
+    mappings and the caches match the oracle."""
+    T, B, H, D, stride, R_pad = 16, 512, 8, 128, 16, 32
+    n_max = R_pad
+    d_qsl = torch.zeros(R_pad + 1, dtype=torch.int32, device=dev())
+    d_pos = torch.zeros(n_max, dtype=torch.int64, device=dev())
+    d_table = torch.zeros((R_pad, stride), dtype=torch.int32, device=dev())
+    d_rs = torch.zeros((R_pad, stride), dtype=torch.int32, device=dev())
+    d_rl = torch.zeros((R_pad, stride), dtype=torch.int32, device=dev())
+    d_nr = torch.zeros(R_pad, dtype=torch.int32, device=dev())
+    key = torch.zeros((1, n_max, H, D), dtype=torch.bfloat16, device=dev())
+    val = torch.zeros_like(key)
+    kc = wl.bf16_normal((1, B, T, H, D), 510, dev())
+    vc = wl.bf16_normal((1, B, T, H, D), 511, dev())
+    slot_p = torch.empty(n_max, dtype=torch.int64, device=dev())
+    slot_r = torch.empty(n_max, dtype=torch.int64, device=dev())
+    err = err_word()
+    side = torch.cuda.Stream()
+
+    def step():
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        kv.kv_slot_mapping_paged(d_qsl, d_pos, d_table, T, B, max_num_tokens=n_max,
+                                 slot_mapping=slot_p, err=err)
+        kv.kv_cache_write(key, val, kc, vc, slot_p, err=err)
+        with torch.cuda.stream(side):
+            kv.kv_slot_mapping_range(d_qsl, d_pos, d_rs, d_rl, d_nr, T, B, max_num_tokens=n_max,
+                                     slot_mapping=slot_r, err=err)
+        cur.wait_stream(side)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    for it, seed in enumerate([21, 22, 23]):
+        R, qsl, pos, table, _, _ = _batch(seed, R_pad, n_max, T, B, stride)
+        rs, rl, nr = _runs(table, R_pad, stride)
+        new_k = wl.bf16_normal((1, n_max, H, D), 610 + it, dev())
+        new_v = wl.bf16_normal((1, n_max, H, D), 710 + it, dev())
+        kc_before, vc_before = bits(kc).copy(), bits(vc).copy()
+        for d, h in ((d_qsl, qsl), (d_pos, pos), (d_table, table), (d_rs, rs), (d_rl, rl),
+                     (d_nr, nr)):
+            d.copy_(torch.from_numpy(h))
+        key.copy_(new_k)
+        val.copy_(new_v)
+        slot_r.fill_(12345)
+        err.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        exp_p, e1 = oracle.slot_mapping_paged(qsl, pos, table, R, n_max, T, B)
+        exp_r, e2 = oracle.slot_mapping_range(qsl, pos, rs, rl, nr, R, n_max, T, B)
+        assert np.array_equal(exp_p, exp_r)  # one layout, two descriptions of it
+        assert np.array_equal(slot_p.cpu().numpy(), exp_p)
+        assert np.array_equal(slot_r.cpu().numpy(), exp_r)
+        e3 = oracle.cache_write(bits(key), bits(val), kc_before, vc_before, exp_p, B, T)
+        assert np.array_equal(bits(kc), kc_before) and np.array_equal(bits(vc), vc_before)
+        assert int(err.item()) == (e1 | e2 | e3) == 0
+
+
 def test_bounded_wait_times_out_and_context_survives():
     """The bounded wait used by the bulk-copy gather gives up on a barrier that
     nothing completes, reports KV_ERR_TIMEOUT, and the next kernels run."""
