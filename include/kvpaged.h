@@ -105,6 +105,10 @@ enum kv_error_bits {
 #define KV_NULL_BLOCK_ID 0
 #define KV_MAX_RANGES_PER_REQ 256   /* [RNG] The Fork Implementation: capped at 256 ranges */
 #define KV_MAX_GATHER_REQS 4096     /* requests per kv_cache_gather(_range) call */
+/* Largest max_num_tokens of one slot-mapping call (paged, range,
+ * context-parallel, fused with the write): 2^31 - 65536, so that token indices
+ * of a whole last tile stay in int32.  Larger values: KV_EINVAL. */
+#define KV_MAX_TOKENS 2147418112
 
 /*
  * kv_slot_mapping_paged -- per-token cache slot through the block table.
@@ -132,8 +136,8 @@ enum kv_error_bits {
  * KV_ERR_BAD_QSL (slot values are then unspecified, but every store stays in
  * bounds).
  * Errors: KV_EINVAL for negative sizes, num_tokens > max_num_tokens,
- * block_size <= 0, num_blocks < 1, table_stride < 0, or a null/misaligned
- * pointer that would be read.
+ * max_num_tokens > KV_MAX_TOKENS, block_size <= 0, num_blocks < 1,
+ * table_stride < 0, or a null/misaligned pointer that would be read.
  */
 int kv_slot_mapping_paged(const int32_t* query_start_loc, const int64_t* positions,
                           const int32_t* block_table, int32_t table_stride, int32_t num_reqs,

@@ -7,7 +7,8 @@ The Python layer only marshals tensors into that ABI (``ops``); the seeded
 synthetic workloads live in ``workloads``.
 """
 from ._lib import (ERR_BITS, KV_EINVAL, KV_EUNSUPPORTED, KV_ECUDA, KV_OK, KVError,
-                   MAX_GATHER_REQS, MAX_RANGES_PER_REQ, NULL_BLOCK_ID, PAD_SLOT_ID, load)
+                   MAX_GATHER_REQS, MAX_RANGES_PER_REQ, MAX_TOKENS, NULL_BLOCK_ID, PAD_SLOT_ID,
+                   load)
 from .ops import (Prepared, kv_cache_gather, kv_cache_gather_range, kv_cache_write, kv_copy_blocks,
                   kv_expand_kernel_blocks, kv_slot_mapping_paged, kv_slot_mapping_paged_cp,
                   kv_slot_mapping_paged_write, kv_slot_mapping_range,
@@ -15,7 +16,7 @@ from .ops import (Prepared, kv_cache_gather, kv_cache_gather_range, kv_cache_wri
 
 __all__ = [
     "ERR_BITS", "KV_EINVAL", "KV_EUNSUPPORTED", "KV_ECUDA", "KV_OK", "KVError",
-    "MAX_GATHER_REQS", "MAX_RANGES_PER_REQ", "NULL_BLOCK_ID", "PAD_SLOT_ID", "load",
+    "MAX_GATHER_REQS", "MAX_RANGES_PER_REQ", "MAX_TOKENS", "NULL_BLOCK_ID", "PAD_SLOT_ID", "load",
     "kv_cache_gather", "kv_cache_write", "kv_expand_kernel_blocks", "kv_slot_mapping_paged",
     "kv_slot_mapping_range", "new_error_word", "kv_table_from_ranges", "kv_cache_gather_range",
     "kv_copy_blocks", "kv_slot_mapping_paged_cp", "kv_slot_mapping_paged_write",

@@ -28,6 +28,7 @@ PAD_SLOT_ID = -1
 NULL_BLOCK_ID = 0
 MAX_RANGES_PER_REQ = 256
 MAX_GATHER_REQS = 4096
+MAX_TOKENS = 2147418112  # largest max_num_tokens of one slot-mapping call (2^31 - 65536)
 
 # Every entry point the header declares, with its argument and result types.
 _P = ctypes.c_void_p

@@ -106,8 +106,8 @@ __device__ __forceinline__ int64_t slot_of(int64_t b, int64_t off, int32_t T, in
 int check_common(const int32_t* qsl, const int64_t* positions, int32_t num_reqs,
                  int32_t num_tokens, int32_t max_num_tokens, int32_t block_size,
                  int64_t num_blocks, const int64_t* slot_mapping) {
-  if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens || block_size <= 0 ||
-      num_blocks < 1)
+  if (num_reqs < 0 || num_tokens < 0 || max_num_tokens < num_tokens ||
+      max_num_tokens > KV_MAX_TOKENS || block_size <= 0 || num_blocks < 1)
     return KV_EINVAL;
   if (num_reqs > 0 && (qsl == nullptr || !aligned(qsl, 4))) return KV_EINVAL;
   if (num_tokens > 0 && (positions == nullptr || !aligned(positions, 8))) return KV_EINVAL;

@@ -144,6 +144,38 @@ def test_next_step_calls_reject_bad_arguments(lib):
                                    N) == -1  # misaligned cache
 
 
+def test_header_constants_match_the_binding():
+    from paged_kv_cache_39_gb300 import _lib
+    text = open(HEADER).read()
+    defs = dict(re.findall(r"^#define\s+(KV_\w+)\s+\(?(-?\d+)\)?", text, flags=re.M))
+    assert int(defs["KV_PAD_SLOT_ID"]) == _lib.PAD_SLOT_ID
+    assert int(defs["KV_NULL_BLOCK_ID"]) == _lib.NULL_BLOCK_ID
+    assert int(defs["KV_MAX_RANGES_PER_REQ"]) == _lib.MAX_RANGES_PER_REQ
+    assert int(defs["KV_MAX_GATHER_REQS"]) == _lib.MAX_GATHER_REQS
+    assert int(defs["KV_MAX_TOKENS"]) == _lib.MAX_TOKENS == (1 << 31) - 65536
+
+
+def test_slot_maps_refuse_max_num_tokens_past_the_limit(lib):
+    """Every slot-mapping entry point refuses max_num_tokens above
+    KV_MAX_TOKENS on the host, before any launch (token indices of a whole
+    last tile must stay in int32)."""
+    from paged_kv_cache_39_gb300 import _lib
+    over = _lib.MAX_TOKENS + 1
+    big = (1 << 31) - 1
+    for n_max in (over, big):
+        assert lib.kv_slot_mapping_paged(0x1000, 0x2000, 0x3000, 8, 1, 0, n_max, 16, 8, 0x4000,
+                                         N, N) == -1
+        assert lib.kv_slot_mapping_range(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 1, 0, n_max,
+                                         16, 8, 0x6000, N, N) == -1
+        assert lib.kv_slot_mapping_paged_cp(0x1000, 0x2000, 0x3000, 8, 1, 0, n_max, 16, 8, 2, 0,
+                                            1, 0x4000, N, N) == -1
+        assert lib.kv_slot_mapping_paged_write(0x1000, 0x2000, 0x3000, 8, 1, 0, n_max, 16, 8, N,
+                                               N, N, N, 1, 8, 128, 0x4000, N, N) == -1
+        assert lib.kv_slot_mapping_range_write(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 1, 0,
+                                               n_max, 16, 8, N, N, N, N, 1, 8, 128, 0x6000, N,
+                                               N) == -1
+
+
 def test_cp_slot_mapping_rejects_bad_arguments(lib):
     assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 0, 0, 1, N, N, N) == -1
     assert lib.kv_slot_mapping_paged_cp(N, N, N, 0, 0, 0, 0, 16, 8, 2, 2, 1, N, N, N) == -1
