@@ -555,10 +555,14 @@ def build_hybrid(torch, kv, wl, dev, small=False):
     return Built("hybrid", desc, launches, N, keep)
 
 
-def build_slotmap(torch, kv, wl, dev, small=False):
+def build_slotmap(torch, kv, wl, dev, small=False, reqs=None):
     """The long-context slot maps alone (1M positions, no caches): a small
-    device footprint for full profiler captures of the two strategies."""
-    w = wl.long_context(num_reqs=2 if small else 8)
+    device footprint for full profiler captures of the two strategies.
+    `reqs` requests of 131072 positions instead of 8 scale the same maps up
+    (4M, 16M positions); beside them a plain copy kernel over the same bytes
+    (positions read, one int64 per token written) gives the floor a kernel of
+    this shape reaches at that size."""
+    w = wl.long_context(num_reqs=reqs or (2 if small else 8))
     T, B = w.block_size, w.num_blocks
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     qsl, pos = t(w.qsl), t(w.positions)
@@ -580,6 +584,9 @@ def build_slotmap(torch, kv, wl, dev, small=False):
                                                 err=err),
                range_bytes(N, N, R, lg.num_ranges), N),
     ]
+    floor_out = torch.empty_like(slot)
+    launches.append(Launch("copy_floor[torch add: positions in, int64 out]", "elementwise_kernel",
+                           lambda: torch.add(pos, 1, out=floor_out), 16 * N, N))
     desc = f"long-context slot maps only: {R} requests x 131072 positions, block_size 16"
     return Built("slotmap", desc, launches, N, dict(err=err))
 
@@ -1283,6 +1290,8 @@ def main():
     ap.add_argument("--small", action="store_true",
                     help="shrink the workload (profiling captures); not a bench line")
     ap.add_argument("--no-detail", action="store_true", help="skip the other workloads")
+    ap.add_argument("--reqs", type=int, default=None,
+                    help="--workload slotmap: requests of 131072 positions (default 8)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--detail-reps", type=int, default=10)
     args = ap.parse_args()
@@ -1410,7 +1419,8 @@ def profile_run(torch, kv, wl, dev, args, rk, flush_buf, stream, peak, kdist):
     """`--workload X` (X not the decode step): the workload's launches in
     order, per-launch events, L2 flushed between steps.  For profiler captures
     and kernel A/B runs; the line is marked as not a bench line."""
-    built = BUILDERS[args.workload](torch, kv, wl, dev, small=args.small)
+    kw = {"reqs": args.reqs} if args.workload == "slotmap" and args.reqs else {}
+    built = BUILDERS[args.workload](torch, kv, wl, dev, small=args.small, **kw)
     for _ in range(args.warmup):
         flush_l2(flush_buf)
         for l in built.launches:
@@ -1418,11 +1428,14 @@ def profile_run(torch, kv, wl, dev, args, rk, flush_buf, stream, peak, kdist):
     torch.cuda.synchronize()
     if int(built.keep["err"].item()) != 0:
         raise SystemExit(f"kernels reported data errors: {int(built.keep['err'].item())}")
-    step_ms, per = time_steps(torch, built, args.steps, flush_buf, stream)
+    step_ms, _ = time_steps(torch, built, args.steps, flush_buf, stream)
+    per = time_each(torch, built, args.steps, flush_buf, stream)
     line = {"not_a_bench_line": f"--workload {args.workload}", "workload": built.desc +
             (" [small]" if args.small else ""), "steps": args.steps,
             "ms_per_step": round(sum(step_ms) / len(step_ms), 4),
-            "kernels": kernel_report(built, per, peak)}
+            "kernels": kernel_report(built, per, peak),
+            "timing": "ms_per_step: the launches back to back, L2 flushed between steps; "
+                      "kernels: each launch alone, L2 flushed before it, CUDA events"}
     if rk.is_main:
         print(json.dumps(line), flush=True)
     kdist.finalize()
