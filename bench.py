@@ -1103,6 +1103,8 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     three prepared calls (paged map -> write, the range map on a second
     branch, as in the device-resident step), and copies both slot mappings and
     the error word back to pinned host memory, where the host checks them.
+    The packed upload ends with zero bytes over the set's error word, so the
+    copy that brings a step's inputs also clears its error word.
 
     Measured the way a pipelined serving loop runs it, inputs prepared one
     step ahead and results checked two steps behind: three buffer sets, and
@@ -1120,12 +1122,14 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     host_src = {"qsl": w.qsl, "pos": w.positions, "table": lay.table, "rs": lay.range_start,
                 "rl": lay.range_len, "nr": lay.num_ranges, "key": k["key"].cpu(),
                 "val": k["val"].cpu()}
-    # one pinned staging buffer, each input at a 256-byte offset
+    # one pinned staging buffer, each input at a 256-byte offset, then 256
+    # zero bytes that land on the set's error word: the upload of a step's
+    # inputs also clears its error word, with no reset of its own in the graph
     offs, total = {}, 0
     for n in names:
         offs[n] = total
         total += -(-k[n].numel() * k[n].element_size() // 256) * 256
-    h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    h_stage = torch.zeros(total + 256, dtype=torch.uint8).pin_memory()
     for n in names:
         nbytes = k[n].numel() * k[n].element_size()
         src = host_src[n]
@@ -1133,7 +1137,7 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
         h_stage[offs[n]:offs[n] + nbytes].copy_(src.contiguous().view(-1).view(torch.uint8))
     T, B, n_max = w.block_size, w.num_blocks, w.max_num_tokens
     n_slot = k["slot_p"].numel()
-    out_bytes = 2 * n_slot * 8 + 256
+    out_bytes = 256 + 2 * n_slot * 8  # error word (256-byte slot), both slot mappings
     exp_p = k["slot_p"].cpu().numpy()
     exp_r = k["slot_r"].cpu().numpy()
     probe = int(np.argmax(exp_p >= 0))
@@ -1142,18 +1146,20 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
         """One set of device buffers, its read-back buffer and prepared calls."""
 
         def __init__(self):
-            self.d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
-            d = {n: self.d_stage[offs[n]:offs[n] + k[n].numel() * k[n].element_size()]
+            # [inputs | error word | slot_p | slot_r]: the upload covers the
+            # inputs and the error word, the read-back the error word and slots
+            buf = torch.zeros(total + out_bytes, dtype=torch.uint8, device=dev)
+            self.d_in, self.d_out = buf[:total + 256], buf[total:]
+            d = {n: buf[offs[n]:offs[n] + k[n].numel() * k[n].element_size()]
                  .view(k[n].dtype).view(k[n].shape) for n in names}
-            self.d_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
             self.h_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
             h = self.h_out.numpy()
-            self.h_slot_p = h[:n_slot * 8].view(np.int64)
-            self.h_slot_r = h[n_slot * 8:2 * n_slot * 8].view(np.int64)
-            self.h_err = h[2 * n_slot * 8:2 * n_slot * 8 + 4].view(np.int32)
-            slot_p = self.d_out[:n_slot * 8].view(torch.int64)
-            slot_r = self.d_out[n_slot * 8:2 * n_slot * 8].view(torch.int64)
-            self.err = self.d_out[2 * n_slot * 8:2 * n_slot * 8 + 4].view(torch.int32)
+            self.h_err = h[:4].view(np.int32)
+            self.h_slot_p = h[256:256 + n_slot * 8].view(np.int64)
+            self.h_slot_r = h[256 + n_slot * 8:256 + 2 * n_slot * 8].view(np.int64)
+            self.err = self.d_out[:4].view(torch.int32)
+            slot_p = self.d_out[256:256 + n_slot * 8].view(torch.int64)
+            slot_r = self.d_out[256 + n_slot * 8:256 + 2 * n_slot * 8].view(torch.int64)
             # validated once; the graphs replay them with the cached pointers
             self.calls = [
                 kv.kv_slot_mapping_paged(d["qsl"], d["pos"], d["table"], T, B,
@@ -1168,10 +1174,9 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
             self.done = torch.cuda.Event()
 
         def upload(self):
-            self.d_stage.copy_(h_stage, non_blocking=True)
+            self.d_in.copy_(h_stage, non_blocking=True)
 
         def compute(self):
-            self.err.zero_()
             paged, rng, write = self.calls
             forked(torch, range_stream, [paged, write], [rng])()
 
@@ -1260,7 +1265,7 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     ms = wall / n_steps * 1e3
     del graphs, serial, sets
     return {"value": round(built.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(out_bytes),
+            "h2d_bytes_per_step": int(total + 256), "d2h_bytes_per_step": int(out_bytes),
             "ms_per_step": round(ms, 4), "steps": n_steps,
             "sync_ms_per_step": round(statistics.median(times) * 1e3, 4),
             "note": "wall time over all steps: each step copies one step's packed inputs "

@@ -45,6 +45,13 @@ def table_stride_for(max_blocks: int, block_size: int) -> int:
     return max(mult, -(-max_blocks // mult) * mult)
 
 
+def range_stride_for(max_runs: int) -> int:
+    """Descriptor capacity per request for a layout whose requests hold at
+    most ``max_runs`` ranges: that cap rounded up to a multiple of 4 (16-byte
+    rows, so a row head loads as one vector), never above the backend's cap."""
+    return min(RANGE_CAP, max(4, -(-max_runs // 4) * 4))
+
+
 def blocks_for(num_tokens: int, block_size: int) -> int:
     """Number of blocks a request holding ``num_tokens`` tokens owns."""
     return -(-num_tokens // block_size)
@@ -281,7 +288,7 @@ def tiny(seed: int = 0) -> Workload:
     nblocks = np.array([blocks_for(int(n), T) for n in lens], dtype=np.int64)
     stride = table_stride_for(int(nblocks.max()), T)
     lay_p = _perm_layout(rng, nblocks, B, R, stride, RANGE_CAP)
-    lay_g = _runs_layout(rng, nblocks, 3, B, R, stride, RANGE_CAP, packed=False)
+    lay_g = _runs_layout(rng, nblocks, 3, B, R, stride, range_stride_for(3), packed=False)
     positions = np.concatenate([np.arange(n, dtype=np.int64) for n in lens])
     N = int(lens.sum())
     n_max = -(-(N + 1) // 256) * 256
@@ -300,7 +307,7 @@ def decode(seed: int = 1, num_blocks: int = 40960, ctx_max: int = 4096) -> Workl
     nblocks = np.array([blocks_for(int(c), T) for c in ctx], dtype=np.int64)
     assert int(nblocks.sum()) < B - 1
     stride = table_stride_for(blocks_for(ctx_max, T), T)
-    lay_g = _runs_layout(rng, nblocks, 4, B, R, stride, RANGE_CAP, packed=False)
+    lay_g = _runs_layout(rng, nblocks, 4, B, R, stride, range_stride_for(4), packed=False)
     positions = (ctx - 1).astype(np.int64)
     g0 = np.zeros(R, dtype=np.int32)
     g1 = ctx.astype(np.int32)
@@ -324,7 +331,8 @@ def mixed(seed: int = 2, num_blocks: int = 49152, decode_ctx_max: int = 4096) ->
     assert int(nblocks.sum()) < num_blocks - 1
     R = n_dec + n_pre
     stride = table_stride_for(int(nblocks.max()), T)
-    lay_g = _runs_layout(rng, nblocks, 8, num_blocks, R, stride, RANGE_CAP, packed=False)
+    lay_g = _runs_layout(rng, nblocks, 8, num_blocks, R, stride, range_stride_for(8),
+                         packed=False)
     positions = np.concatenate(
         [(dec_ctx - 1).astype(np.int64)]
         + [np.arange(int(c), int(c) + int(n), dtype=np.int64) for c, n in zip(pre_prior, pre_len)])
@@ -345,7 +353,7 @@ def long_context(seed: int = 3, num_reqs: int = 8, tokens_per_req: int = 131072)
     nblocks = np.full(num_reqs, per, dtype=np.int64)
     stride = table_stride_for(per, T)
     lay_p = _perm_layout(rng, nblocks, B, num_reqs, stride, None)
-    lay_g = _runs_layout(rng, nblocks, 16, B, num_reqs, stride, RANGE_CAP, packed=True)
+    lay_g = _runs_layout(rng, nblocks, 16, B, num_reqs, stride, range_stride_for(16), packed=True)
     positions = np.tile(np.arange(tokens_per_req, dtype=np.int64), num_reqs)
     N = num_reqs * tokens_per_req
     g0 = np.zeros(num_reqs, dtype=np.int32)
