@@ -45,7 +45,10 @@ __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* 
   }
   const int32_t* q = staged ? s_qsl : a.qsl;
   if (n > 0) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    // 64-bit thread index: a grid of one CTA per few tokens passes 2^32
+    // threads below KV_MAX_TOKENS
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += step)
       if (q[i] > q[i + 1]) err |= KV_ERR_BAD_QSL;
     if (blockIdx.x == 0 && threadIdx.x == 0 && (q[0] < 0 || q[n] > a.num_tokens))
       err |= KV_ERR_BAD_QSL;

@@ -280,9 +280,9 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   // descriptor-row validation, every request, grid-wide: the thread's first
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
-  const int sweep0 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
-  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, sweep0, rstride, vec4);
+  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, (int)sweep0, rstride, vec4);
 
   RangeWindow win;  // this lane's last resolved range
   ReqSpan last_r;
@@ -383,8 +383,9 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   }
   if (sweep0 < a.num_reqs) {
     if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    for (int r = sweep0 + gridDim.x * blockDim.x; r < a.num_reqs; r += gridDim.x * blockDim.x)
-      if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+      if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
   }
   report(a.err, err);
 }
@@ -516,9 +517,9 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
   // descriptor-row validation, every request, grid-wide: the thread's first
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
-  const int sweep0 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
-  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, sweep0, rstride, vec4);
+  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, (int)sweep0, rstride, vec4);
 
   // Requests of this tile: [st_lo, st_lo + st_n) when at most kStageReqs
   // (every thread computes the same, CTA-uniform values).
@@ -622,8 +623,9 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
   }
   if (sweep0 < a.num_reqs) {
     if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    for (int r = sweep0 + gridDim.x * blockDim.x; r < a.num_reqs; r += gridDim.x * blockDim.x)
-      if (range_row_malformed(num_ranges, range_len, r, rstride)) err |= KV_ERR_BAD_RANGE;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+      if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
   }
   report(a.err, err);
 }

@@ -204,10 +204,10 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   uint32_t err = 0;
   // descriptor-row validation, one row per thread grid-wide (range form): the
   // first row is requested now and checked at the end
-  const int sweep0 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
   if constexpr (Lookup::kRows) {
-    if (sweep0 < a.num_reqs) first_row.load(lk.count, lk.len, sweep0, lk.stride, vec4);
+    if (sweep0 < a.num_reqs) first_row.load(lk.count, lk.len, (int)sweep0, lk.stride, vec4);
   }
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err, [&] {
     if (live && p >= 0) a.bs.divmod(p, lb, off);
@@ -247,9 +247,9 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   if constexpr (Lookup::kRows) {
     if (sweep0 < a.num_reqs) {
       if (first_row.malformed(lk.len, lk.stride)) err |= KV_ERR_BAD_RANGE;
-      for (int r = sweep0 + gridDim.x * blockDim.x; r < a.num_reqs;
-           r += gridDim.x * blockDim.x)
-        if (range_row_malformed(lk.count, lk.len, r, lk.stride)) err |= KV_ERR_BAD_RANGE;
+      const int64_t step = (int64_t)gridDim.x * blockDim.x;
+      for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+        if (range_row_malformed(lk.count, lk.len, (int)r, lk.stride)) err |= KV_ERR_BAD_RANGE;
     }
   }
   report(a.err, err);

@@ -634,6 +634,67 @@ def test_range_staged_with_qsl_in_global_memory():
     assert np.array_equal(s, exp_s)
 
 
+def test_slot_maps_at_the_token_limit():
+    """max_num_tokens = KV_MAX_TOKENS (2^31 - 65536, a 17 GB slot buffer):
+    the largest launch every slot map accepts.  The last tiles' token indices
+    come within one tile of 2^31, and the fused calls' grids (one CTA per 8
+    tokens) pass 2^32 threads, so every grid-wide index must be 64-bit.  The
+    real tokens match the oracle and every padded slot reads PAD (checked on
+    the device)."""
+    rng = np.random.default_rng(31000)
+    T, B, H, D, R = 16, 512, 1, 8, 4
+    lens = np.array([250, 1, 0, 300])
+    qsl = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(qsl[-1])
+    pos = np.concatenate([np.arange(n) + int(rng.integers(0, 64)) for n in lens]).astype(np.int64)
+    stride = 32
+    perm = rng.permutation(np.arange(1, B))
+    table = perm[:R * stride].reshape(R, stride).astype(np.int32)
+    rs, rl = table.copy(), np.ones_like(table)  # one range per block
+    nr = np.full(R, stride, np.int32)
+    n_max = kv.MAX_TOKENS
+    slot = torch.empty(n_max, dtype=torch.int64, device=dev())
+    exp, exp_e = oracle.slot_mapping_paged(qsl, pos, table, N, N, T, B)
+    exp_r, exp_re = oracle.slot_mapping_range(qsl, pos, rs, rl, nr, N, N, T, B)
+    assert np.array_equal(exp, exp_r) and exp_e == exp_re == 0
+    exp_cp, exp_cpe = oracle.slot_mapping_paged_cp(qsl, pos, table, N, N, T, B, 2, 1, 4)
+    key = wl.bf16_normal((1, N, H, D), 310).to(dev())
+    kc = torch.zeros((1, B, T, H, D), dtype=torch.bfloat16, device=dev())
+    vc = torch.zeros_like(kc)
+    calls = {
+        "paged": (lambda e: kv.kv_slot_mapping_paged(cuda(qsl), cuda(pos), cuda(table), T, B,
+                                                     max_num_tokens=n_max, slot_mapping=slot,
+                                                     err=e), exp),
+        "range": (lambda e: kv.kv_slot_mapping_range(cuda(qsl), cuda(pos), cuda(rs), cuda(rl),
+                                                     cuda(nr), T, B, max_num_tokens=n_max,
+                                                     slot_mapping=slot, err=e), exp),
+        "cp": (lambda e: kv.kv_slot_mapping_paged_cp(cuda(qsl), cuda(pos), cuda(table), T, B, 2,
+                                                     1, 4, max_num_tokens=n_max,
+                                                     slot_mapping=slot, err=e), exp_cp),
+        "paged_write": (lambda e: kv.kv_slot_mapping_paged_write(
+            cuda(qsl), cuda(pos), cuda(table), T, B, key, key, kc, vc, max_num_tokens=n_max,
+            slot_mapping=slot, err=e), exp),
+        "range_write": (lambda e: kv.kv_slot_mapping_range_write(
+            cuda(qsl), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B, key, key, kc, vc,
+            max_num_tokens=n_max, slot_mapping=slot, err=e), exp),
+    }
+    for name, (call, want) in calls.items():
+        slot[:N].fill_(12345)
+        slot[-4096:].fill_(12345)
+        e = err_word()
+        call(e)
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0, name
+        assert np.array_equal(slot[:N].cpu().numpy(), want), name
+        assert bool((slot[N:] == -1).all()), name
+    ek = np.zeros((1, B, T, H, D), np.uint16)
+    ev = ek.copy()
+    assert oracle.cache_write(bits(key), bits(key), ek, ev, exp, B, T) == 0
+    assert np.array_equal(bits(kc), ek) and np.array_equal(bits(vc), ev)
+    del slot
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("pad", [0, 700_000])
 def test_range_lengths_past_int32(pad):
     """Ranges of 2^27 and 2^30 blocks (cumulative block counts past 2^31, so
