@@ -247,6 +247,14 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Grid-wide thread index and thread count, 64-bit: a grid of one CTA per few
+// tokens passes 2^32 threads below KV_MAX_TOKENS.  Cheap to recompute (special
+// registers), so kernels recompute them where needed instead of holding them.
+__device__ __forceinline__ int64_t grid_thread() {
+  return (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+}
+__device__ __forceinline__ int64_t grid_threads() { return (int64_t)gridDim.x * blockDim.x; }
+
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

@@ -24,14 +24,13 @@ struct SlotArgs {
   int32_t* err;
 };
 
-// Stage query_start_loc in shared memory when it fits; validate it grid-wide.
+// Stage query_start_loc in shared memory when it fits.
 // `overlap()` runs once the thread's first staging load is in flight and
 // before the barrier: work that waits on other loads (a position) can then
 // issue its own loads without holding the staging back.
 template <class Overlap>
 __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
-                                                    bool staged, uint32_t& err,
-                                                    Overlap&& overlap) {
+                                                    bool staged, Overlap&& overlap) {
   const int n = a.num_reqs;
   if (staged) {
     const int i0 = threadIdx.x;
@@ -43,22 +42,24 @@ __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* 
   } else {
     overlap();
   }
-  const int32_t* q = staged ? s_qsl : a.qsl;
-  if (n > 0) {
-    // 64-bit thread index: a grid of one CTA per few tokens passes 2^32
-    // threads below KV_MAX_TOKENS
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += step)
-      if (q[i] > q[i + 1]) err |= KV_ERR_BAD_QSL;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && (q[0] < 0 || q[n] > a.num_tokens))
-      err |= KV_ERR_BAD_QSL;
-  }
-  return q;
+  return staged ? s_qsl : a.qsl;
+}
+
+// Validate query_start_loc grid-wide (q: the staged or the global copy):
+// non-decreasing, q[0] >= 0, q[num_reqs] <= num_tokens.  A kernel calls it
+// where its registers are least needed.
+__device__ __forceinline__ void check_qsl(const SlotArgs& a, const int32_t* q, uint32_t& err) {
+  const int n = a.num_reqs;
+  if (n <= 0) return;
+  for (int64_t i = grid_thread(); i < n; i += grid_threads())
+    if (q[i] > q[i + 1]) err |= KV_ERR_BAD_QSL;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (q[0] < 0 || q[n] > a.num_tokens))
+    err |= KV_ERR_BAD_QSL;
 }
 
 __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
-                                                    bool staged, uint32_t& err) {
-  return stage_qsl(a, s_qsl, staged, err, [] {});
+                                                    bool staged) {
+  return stage_qsl(a, s_qsl, staged, [] {});
 }
 
 // Request owning token t (t < num_tokens), or -1 when no span covers it.

@@ -61,7 +61,7 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
     p[k] = t < a.num_tokens ? a.positions[t] : 0;
   }
   uint32_t err = 0;
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
   // phase 1: table index of every token of the thread (-1: PAD without lookup)
   int64_t idx[kTokPerThread], off[kTokPerThread];
   int last_r = -1;
@@ -125,6 +125,7 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
       a.slot_mapping[t] = slot_of(blk[k], off[k], a.bs.size, a.num_blocks, err);
     }
   }
+  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 
@@ -269,7 +270,7 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
     }
   }
   uint32_t err = 0;
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) s_pos[k][threadIdx.x] = p[k];
   // the warp's scanned chunk 0 of request c_r (c_nr < 0: malformed row)
@@ -280,9 +281,9 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   // descriptor-row validation, every request, grid-wide: the thread's first
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
-  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
-  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, (int)sweep0, rstride, vec4);
+  if (grid_thread() < a.num_reqs)
+    first_row.load(num_ranges, range_len, (int)grid_thread(), rstride, vec4);
 
   RangeWindow win;  // this lane's last resolved range
   ReqSpan last_r;
@@ -381,12 +382,12 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
       a.slot_mapping[t] =
           found ? slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err) : kPad;
   }
-  if (sweep0 < a.num_reqs) {
+  if (first_row.r >= 0) {  // this thread's first row was loaded (grid_thread() < num_reqs)
     if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+    for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
       if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
   }
+  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 
@@ -512,14 +513,14 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
     else s_pos[k][threadIdx.x] = 0;
   }
   uint32_t err = 0;
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err);
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
 
   // descriptor-row validation, every request, grid-wide: the thread's first
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
-  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
-  if (sweep0 < a.num_reqs) first_row.load(num_ranges, range_len, (int)sweep0, rstride, vec4);
+  if (grid_thread() < a.num_reqs)
+    first_row.load(num_ranges, range_len, (int)grid_thread(), rstride, vec4);
 
   // Requests of this tile: [st_lo, st_lo + st_n) when at most kStageReqs
   // (every thread computes the same, CTA-uniform values).
@@ -621,12 +622,12 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
       a.slot_mapping[t] = slot;
     }
   }
-  if (sweep0 < a.num_reqs) {
+  if (first_row.r >= 0) {  // this thread's first row was loaded (grid_thread() < num_reqs)
     if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+    for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
       if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
   }
+  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 

@@ -204,12 +204,12 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   uint32_t err = 0;
   // descriptor-row validation, one row per thread grid-wide (range form): the
   // first row is requested now and checked at the end
-  const int64_t sweep0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 64-bit: see stage_qsl
   RangeRowCheck first_row;
   if constexpr (Lookup::kRows) {
-    if (sweep0 < a.num_reqs) first_row.load(lk.count, lk.len, (int)sweep0, lk.stride, vec4);
+    if (grid_thread() < a.num_reqs)
+      first_row.load(lk.count, lk.len, (int)grid_thread(), lk.stride, vec4);
   }
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, err, [&] {
+  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, [&] {
     if (live && p >= 0) a.bs.divmod(p, lb, off);
     if constexpr (Lookup::kNeedsBlock) {
       if (guess && p >= 0) g_pre = lk.prefetch(t, lb);
@@ -245,13 +245,15 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   }
 
   if constexpr (Lookup::kRows) {
-    if (sweep0 < a.num_reqs) {
+    if (first_row.r >= 0) {  // this thread's first row was loaded
       if (first_row.malformed(lk.len, lk.stride)) err |= KV_ERR_BAD_RANGE;
-      const int64_t step = (int64_t)gridDim.x * blockDim.x;
-      for (int64_t r = sweep0 + step; r < a.num_reqs; r += step)
+      for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
         if (range_row_malformed(lk.count, lk.len, (int)r, lk.stride)) err |= KV_ERR_BAD_RANGE;
     }
   }
+  // the grid-wide query_start_loc check last, once the rows are out of the
+  // registers (q: the staged copy stays valid to the end of the kernel)
+  check_qsl(a, q, err);
   report(a.err, err);
 }
 
