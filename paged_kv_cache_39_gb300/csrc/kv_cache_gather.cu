@@ -249,8 +249,12 @@ cache_gather_range_kernel(GatherArgs a, const int32_t* __restrict__ range_start,
   __shared__ int64_t s_warp_sum[kGatherStaticSmem / sizeof(int64_t)];
   uint32_t err = 0;
   // descriptor-row validation, every request, grid-wide
-  for (int64_t r = grid_thread(); r < a.num_reqs; r += grid_threads())
-    if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+  {
+    unsigned r, step;
+    if (grid_first(a.num_reqs, r, step)) do {
+        if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+      } while (grid_next(a.num_reqs, r, step));
+  }
   const int64_t total = packed_offsets(a, s_off, s_start, s_warp_sum, err);
   const int64_t rows = total < a.out_rows ? total : a.out_rows;
   RangeResolver res{range_start, range_len, num_ranges, rstride};

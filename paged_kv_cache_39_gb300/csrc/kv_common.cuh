@@ -247,13 +247,28 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Grid-wide thread index and thread count, 64-bit: a grid of one CTA per few
-// tokens passes 2^32 threads below KV_MAX_TOKENS.  Cheap to recompute (special
-// registers), so kernels recompute them where needed instead of holding them.
-__device__ __forceinline__ int64_t grid_thread() {
-  return (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// Grid-stride walk of [0, n) (n <= INT32_MAX), this thread's share, safe for
+// grids of more than 2^32 threads: the CTA's first index and the grid's
+// thread count are formed as 64-bit products (one wide multiply each, no
+// division); past the test the index is below n + blockDim, so the walk runs
+// in 32 bits.  A grid that covers n walks once (step n), else its thread
+// count is below n, and i + step is formed only while it stays below n.
+//   unsigned i, step;
+//   if (grid_first(n, i, step)) do { ... i ... } while (grid_next(n, i, step));
+__device__ __forceinline__ bool grid_first(int n, unsigned& i, unsigned& step) {
+  if (n <= 0) return false;
+  const uint64_t base = (uint64_t)blockIdx.x * blockDim.x;
+  if (base >= (uint64_t)n) return false;
+  i = (unsigned)base + threadIdx.x;
+  const uint64_t total = (uint64_t)gridDim.x * blockDim.x;
+  step = total >= (uint64_t)n ? (unsigned)n : (unsigned)total;
+  return i < (unsigned)n;
 }
-__device__ __forceinline__ int64_t grid_threads() { return (int64_t)gridDim.x * blockDim.x; }
+__device__ __forceinline__ bool grid_next(int n, unsigned& i, unsigned step) {
+  if (i >= (unsigned)n - step) return false;
+  i += step;
+  return true;
+}
 
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;

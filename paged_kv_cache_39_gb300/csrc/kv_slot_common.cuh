@@ -46,14 +46,14 @@ __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* 
 }
 
 // Validate query_start_loc grid-wide (q: the staged or the global copy):
-// non-decreasing, q[0] >= 0, q[num_reqs] <= num_tokens.  A kernel calls it
-// where its registers are least needed.
+// non-decreasing, q[0] >= 0, q[num_reqs] <= num_tokens.
 __device__ __forceinline__ void check_qsl(const SlotArgs& a, const int32_t* q, uint32_t& err) {
   const int n = a.num_reqs;
-  if (n <= 0) return;
-  for (int64_t i = grid_thread(); i < n; i += grid_threads())
-    if (q[i] > q[i + 1]) err |= KV_ERR_BAD_QSL;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && (q[0] < 0 || q[n] > a.num_tokens))
+  unsigned i, step;
+  if (grid_first(n, i, step)) do {
+      if (q[i] > q[i + 1]) err |= KV_ERR_BAD_QSL;
+    } while (grid_next(n, i, step));
+  if (n > 0 && blockIdx.x == 0 && threadIdx.x == 0 && (q[0] < 0 || q[n] > a.num_tokens))
     err |= KV_ERR_BAD_QSL;
 }
 

@@ -62,6 +62,7 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
+  check_qsl(a, q, err);  // in the shadow of the position loads
   // phase 1: table index of every token of the thread (-1: PAD without lookup)
   int64_t idx[kTokPerThread], off[kTokPerThread];
   int last_r = -1;
@@ -125,7 +126,6 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
       a.slot_mapping[t] = slot_of(blk[k], off[k], a.bs.size, a.num_blocks, err);
     }
   }
-  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 
@@ -271,6 +271,7 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
+  check_qsl(a, q, err);  // in the shadow of the position loads
 #pragma unroll
   for (int k = 0; k < kTokPerThread; ++k) s_pos[k][threadIdx.x] = p[k];
   // the warp's scanned chunk 0 of request c_r (c_nr < 0: malformed row)
@@ -282,8 +283,11 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
   RangeRowCheck first_row;
-  if (grid_thread() < a.num_reqs)
-    first_row.load(num_ranges, range_len, (int)grid_thread(), rstride, vec4);
+  {
+    unsigned r0, step;
+    if (grid_first(a.num_reqs, r0, step))
+      first_row.load(num_ranges, range_len, (int)r0, rstride, vec4);
+  }
 
   RangeWindow win;  // this lane's last resolved range
   ReqSpan last_r;
@@ -382,12 +386,14 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
       a.slot_mapping[t] =
           found ? slot_of(win.start + (lb - win.lo), off, a.bs.size, a.num_blocks, err) : kPad;
   }
-  if (first_row.r >= 0) {  // this thread's first row was loaded (grid_thread() < num_reqs)
-    if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
-      if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+  {
+    unsigned r, step;  // this thread's rows: the first was loaded above
+    if (grid_first(a.num_reqs, r, step)) {
+      if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
+      while (grid_next(a.num_reqs, r, step))
+        if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+    }
   }
-  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 
@@ -514,13 +520,17 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
   }
   uint32_t err = 0;
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem);
+  check_qsl(a, q, err);  // in the shadow of the position loads
 
   // descriptor-row validation, every request, grid-wide: the thread's first
   // row is requested now and checked after the token loop, so the check costs
   // no round trip on the loop's critical path
   RangeRowCheck first_row;
-  if (grid_thread() < a.num_reqs)
-    first_row.load(num_ranges, range_len, (int)grid_thread(), rstride, vec4);
+  {
+    unsigned r0, step;
+    if (grid_first(a.num_reqs, r0, step))
+      first_row.load(num_ranges, range_len, (int)r0, rstride, vec4);
+  }
 
   // Requests of this tile: [st_lo, st_lo + st_n) when at most kStageReqs
   // (every thread computes the same, CTA-uniform values).
@@ -622,12 +632,14 @@ slot_mapping_range_staged_kernel(SlotArgs a, const int32_t* __restrict__ range_s
       a.slot_mapping[t] = slot;
     }
   }
-  if (first_row.r >= 0) {  // this thread's first row was loaded (grid_thread() < num_reqs)
-    if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
-    for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
-      if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+  {
+    unsigned r, step;  // this thread's rows: the first was loaded above
+    if (grid_first(a.num_reqs, r, step)) {
+      if (first_row.malformed(range_len, rstride)) err |= KV_ERR_BAD_RANGE;
+      while (grid_next(a.num_reqs, r, step))
+        if (range_row_malformed(num_ranges, range_len, (int)r, rstride)) err |= KV_ERR_BAD_RANGE;
+    }
   }
-  check_qsl(a, q, err);  // grid-wide, last: its registers are free by now
   report(a.err, err);
 }
 

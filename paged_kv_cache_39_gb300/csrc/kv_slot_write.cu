@@ -206,8 +206,9 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   // first row is requested now and checked at the end
   RangeRowCheck first_row;
   if constexpr (Lookup::kRows) {
-    if (grid_thread() < a.num_reqs)
-      first_row.load(lk.count, lk.len, (int)grid_thread(), lk.stride, vec4);
+    unsigned r0, step;
+    if (grid_first(a.num_reqs, r0, step))
+      first_row.load(lk.count, lk.len, (int)r0, lk.stride, vec4);
   }
   const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, [&] {
     if (live && p >= 0) a.bs.divmod(p, lb, off);
@@ -215,6 +216,7 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
       if (guess && p >= 0) g_pre = lk.prefetch(t, lb);
     }
   });
+  check_qsl(a, q, err);
 
   int64_t b = kNull, slot = kPad;
   if (live) {
@@ -245,15 +247,13 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
   }
 
   if constexpr (Lookup::kRows) {
-    if (first_row.r >= 0) {  // this thread's first row was loaded
+    unsigned r, step;  // this thread's rows: the first was loaded above
+    if (grid_first(a.num_reqs, r, step)) {
       if (first_row.malformed(lk.len, lk.stride)) err |= KV_ERR_BAD_RANGE;
-      for (int64_t r = grid_thread() + grid_threads(); r < a.num_reqs; r += grid_threads())
+      while (grid_next(a.num_reqs, r, step))
         if (range_row_malformed(lk.count, lk.len, (int)r, lk.stride)) err |= KV_ERR_BAD_RANGE;
     }
   }
-  // the grid-wide query_start_loc check last, once the rows are out of the
-  // registers (q: the staged copy stays valid to the end of the kernel)
-  check_qsl(a, q, err);
   report(a.err, err);
 }
 
