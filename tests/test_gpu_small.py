@@ -695,6 +695,50 @@ def test_slot_maps_at_the_token_limit():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("kind", ["paged_write", "range_write"])
+def test_grid_wide_checks_on_grids_past_2_32_threads(kind):
+    """The fused calls at max_num_tokens = 2^27: one CTA per 8 tokens is
+    2^24 CTAs, 2^32 threads.  Their grid-wide checks (query_start_loc, and the
+    range form's descriptor rows) must still visit the last requests: a
+    decrease of query_start_loc near the end and a malformed last row are
+    reported, exactly as the oracle reports them."""
+    rng = np.random.default_rng(32000)
+    T, B, H, D, R = 16, 8192, 1, 8, 5000
+    n_max = 1 << 27
+    qsl = np.arange(R + 1, dtype=np.int32)
+    qsl[R - 2] = qsl[R - 1] + 1  # decreasing at R - 2
+    pos = rng.integers(0, 4 * T, size=R).astype(np.int64)
+    table = rng.integers(1, B, size=(R, 4)).astype(np.int32)
+    rs, rl = table.copy(), np.ones_like(table)
+    nr = np.full(R, 4, np.int32)
+    nr[R - 1] = 5  # more ranges than the row holds
+    if kind == "paged_write":
+        _, exp_e = oracle.slot_mapping_paged(qsl, pos, table, R, R, T, B)
+    else:
+        _, exp_e = oracle.slot_mapping_range(qsl, pos, rs, rl, nr, R, R, T, B)
+    assert exp_e & kv.ERR_BITS["BAD_QSL"]
+    assert kind == "paged_write" or exp_e & kv.ERR_BITS["BAD_RANGE"]
+    key = torch.zeros((1, R, H, D), dtype=torch.bfloat16, device=dev())
+    kc = torch.zeros((1, B, T, H, D), dtype=torch.bfloat16, device=dev())
+    vc = torch.zeros_like(kc)
+    slot = torch.empty(n_max, dtype=torch.int64, device=dev())
+    e = err_word()
+    if kind == "paged_write":
+        kv.kv_slot_mapping_paged_write(cuda(qsl), cuda(pos), cuda(table), T, B, key, key, kc, vc,
+                                       max_num_tokens=n_max, slot_mapping=slot, err=e)
+    else:
+        kv.kv_slot_mapping_range_write(cuda(qsl), cuda(pos), cuda(rs), cuda(rl), cuda(nr), T, B,
+                                       key, key, kc, vc, max_num_tokens=n_max,
+                                       slot_mapping=slot, err=e)
+    torch.cuda.synchronize()
+    got = int(e.item())
+    check = kv.ERR_BITS["BAD_QSL"] | kv.ERR_BITS["BAD_RANGE"]
+    assert got & check == exp_e & check
+    assert bool((slot[R:] == -1).all())  # the padded tail, whatever the bad spans gave
+    del slot
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("pad", [0, 700_000])
 def test_range_lengths_past_int32(pad):
     """Ranges of 2^27 and 2^30 blocks (cumulative block counts past 2^31, so
