@@ -645,6 +645,24 @@ def test_table_stride_alignment():
     assert wl.table_stride_for(1, 128) == 1
 
 
+def test_range_stride_for():
+    # the run cap rounded up to 16-byte rows, never past the backend's cap
+    assert [wl.range_stride_for(m) for m in (1, 3, 4, 5, 8, 16, 255, 256, 300)] == \
+        [4, 4, 4, 8, 8, 16, 256, 256, 256]
+
+
+@pytest.mark.parametrize("name,cap", [("tiny", 3), ("decode", 4), ("mixed", 8), ("long", 16)])
+def test_descriptor_rows_sized_to_the_run_cap(name, cap):
+    """Layout G's descriptor rows hold the layout's run cap (rounded up to a
+    multiple of 4), and every request's ranges fit; layout P keeps 256."""
+    w = wl.CONFIGS[name]()
+    g = w.layouts["G"]
+    assert g.range_start.shape[1] == g.range_len.shape[1] == wl.range_stride_for(cap)
+    assert 1 <= g.num_ranges[g.num_ranges > 0].min() and g.num_ranges.max() <= cap
+    if "P" in w.layouts and w.layouts["P"].range_start is not None:
+        assert w.layouts["P"].range_start.shape[1] == wl.RANGE_CAP
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode", "mixed", "long"])
 def test_workload_structure(name):
     w = wl.CONFIGS[name]()
