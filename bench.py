@@ -695,6 +695,28 @@ def host_decode_state(wl, seed=1):
     return w, lay, kc_h, vc_h, key_h, val_h
 
 
+def host_cpu():
+    """The host CPU's model as the OS reports it ("unknown" when it does not)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        m = re.search(r"^model name\s*:\s*(.+)$", info, flags=re.M)
+        if m:
+            return m.group(1).strip()
+        # Arm cores name the implementer and the part number instead
+        impl = re.search(r"^CPU implementer\s*:\s*(\S+)", info, flags=re.M)
+        part = re.search(r"^CPU part\s*:\s*(\S+)", info, flags=re.M)
+        if impl and part:
+            parts = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+                     ("0x41", "0xd0c"): "Arm Neoverse N1"}
+            key = (impl.group(1).lower(), part.group(1).lower())
+            return parts.get(key, f"{platform.machine()} implementer {key[0]} part {key[1]}")
+    except OSError:
+        pass
+    return platform.processor() or platform.machine() or "unknown"
+
+
 def cpu_baseline(seconds, rounds=5):
     """The oracle's headline step on one host core, timed in the pages' host-bench
     manner: `rounds` rounds, one warm-up call per round, then whole steps for
@@ -722,7 +744,8 @@ def cpu_baseline(seconds, rounds=5):
             "sample": f"{steps_total} whole headline steps of the oracle (paged and range slot "
                       f"maps and the KV write of all 256 decode tokens) in {rounds} rounds, "
                       f"single-threaded, {el_total:.1f} s",
-            "host_cores": os.cpu_count()}
+            "host_cores": os.cpu_count(), "host_cpu": host_cpu(),
+            "cores_note": f"1 of {os.cpu_count()} cores"}
 
 
 def oracle_rows(seconds_cap=4.0):
@@ -858,7 +881,8 @@ def run_reference(args, rk):
             "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
             "config": {"workload": DECODE_DESC, "parallelism": "host cores, rank 0"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "host_cores": os.cpu_count(),
+                             "host_cpu": host_cpu()},
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
