@@ -72,7 +72,8 @@ slot_mapping_paged_kernel(SlotArgs a, const int32_t* __restrict__ table, int32_t
     idx[k] = -1;
     off[k] = 0;
     if (t < a.num_tokens) {
-      const int r = request_of_cached(q, a.num_reqs, t, last_r);
+      const int r = kTokPerThread == 1 ? request_of_guess(q, a.num_reqs, t)
+                                       : request_of_cached(q, a.num_reqs, t, last_r);
       if (r >= 0) {
         if (p[k] < 0) {
           err |= KV_ERR_BAD_POSITION;
@@ -296,7 +297,9 @@ slot_mapping_range_kernel(SlotArgs a, const int32_t* __restrict__ range_start,
     const int32_t t = base + k * kThreads;
     const int64_t pk = s_pos[k][threadIdx.x];
     // every lane of the warp reaches the votes and shuffles below: no early exit
-    const int r = t < a.num_tokens ? request_of_cached(q, a.num_reqs, t, last_r) : -1;
+    const int r = t >= a.num_tokens   ? -1
+                  : kTokPerThread == 1 ? request_of_guess(q, a.num_reqs, t)
+                                       : request_of_cached(q, a.num_reqs, t, last_r);
     bool need = false;
     if (r >= 0) {
       if (pk < 0) err |= KV_ERR_BAD_POSITION;

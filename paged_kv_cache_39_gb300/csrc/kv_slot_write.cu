@@ -220,7 +220,7 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
 
   int64_t b = kNull, slot = kPad;
   if (live) {
-    const int r = request_of(q, a.num_reqs, t);
+    const int r = request_of_guess(q, a.num_reqs, t);
     if (r >= 0) {
       if (p < 0) {
         err |= KV_ERR_BAD_POSITION;
