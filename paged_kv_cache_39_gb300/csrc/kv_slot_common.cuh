@@ -28,16 +28,29 @@ struct SlotArgs {
 // `overlap()` runs once the thread's first staging load is in flight and
 // before the barrier: work that waits on other loads (a position) can then
 // issue its own loads without holding the staging back.
-template <class Overlap>
+// Up to kStageLoads entries per thread are requested before any is stored,
+// so up to kStageLoads * blockDim entries arrive in one round trip (a
+// 256-request batch has 257: with one load per thread before the store,
+// thread 0's second load waited on its first, and the barrier on both).
+template <int kStageLoads = 4, class Overlap>
 __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
                                                     bool staged, Overlap&& overlap) {
   const int n = a.num_reqs;
   if (staged) {
     const int i0 = threadIdx.x;
-    const int32_t v0 = i0 <= n ? a.qsl[i0] : 0;
+    int32_t v[kStageLoads];
+#pragma unroll
+    for (int u = 0; u < kStageLoads; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      v[u] = i <= n ? a.qsl[i] : 0;
+    }
     overlap();
-    if (i0 <= n) s_qsl[i0] = v0;
-    for (int i = i0 + blockDim.x; i <= n; i += blockDim.x) s_qsl[i] = a.qsl[i];
+#pragma unroll
+    for (int u = 0; u < kStageLoads; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i <= n) s_qsl[i] = v[u];
+    }
+    for (int i = i0 + kStageLoads * (int)blockDim.x; i <= n; i += blockDim.x) s_qsl[i] = a.qsl[i];
     __syncthreads();
   } else {
     overlap();
@@ -59,7 +72,7 @@ __device__ __forceinline__ void check_qsl(const SlotArgs& a, const int32_t* q, u
 
 __device__ __forceinline__ const int32_t* stage_qsl(const SlotArgs& a, int32_t* s_qsl,
                                                     bool staged) {
-  return stage_qsl(a, s_qsl, staged, [] {});
+  return stage_qsl<4>(a, s_qsl, staged, [] {});
 }
 
 // Request owning token t (t < num_tokens), or -1 when no span covers it.

@@ -210,7 +210,7 @@ slot_write_kernel(SlotArgs a, Lookup lk, RowArgs w, bool qsl_in_smem, bool vec4)
     if (grid_first(a.num_reqs, r0, step))
       first_row.load(lk.count, lk.len, (int)r0, lk.stride, vec4);
   }
-  const int32_t* q = stage_qsl(a, s_qsl, qsl_in_smem, [&] {
+  const int32_t* q = stage_qsl<2>(a, s_qsl, qsl_in_smem, [&] {  // 2: 64 registers
     if (live && p >= 0) a.bs.divmod(p, lb, off);
     if constexpr (Lookup::kNeedsBlock) {
       if (guess && p >= 0) g_pre = lk.prefetch(t, lb);
