@@ -234,6 +234,47 @@ def test_range_staging_boundary(per_req, pad, S):
     assert np.array_equal(s, exp_s)
 
 
+def test_decode_batch_past_the_staging_limit():
+    """10000 one-token requests: query_start_loc stays in global memory (more
+    than the slot maps' 8191 and the fused calls' 2047 staged requests), and
+    every thread's "request t owns token t" check hits there, the search
+    never runs.  All four calls against the oracle."""
+    rng = np.random.default_rng(7100)
+    R, T, H, D, stride = 10000, 16, 1, 8, 4
+    B = R * stride + 1
+    q = np.arange(R + 1, dtype=np.int32)
+    pos = rng.integers(0, stride * T, size=R).astype(np.int64)
+    table = rng.permutation(np.arange(1, B)).astype(np.int32).reshape(R, stride)
+    rs, rl = table.copy(), np.ones_like(table)
+    nr = np.full(R, stride, np.int32)
+    n_max = R + 100
+    exp_s, exp_e = oracle.slot_mapping_paged(q, pos, table, R, n_max, T, B)
+    assert exp_e == 0 and (exp_s[:R] >= 0).all()
+    s, e = run_paged(q, pos, table, R, n_max, T, B)
+    assert e == 0 and np.array_equal(s, exp_s)
+    s, e = run_range(q, pos, rs, rl, nr, R, n_max, T, B)
+    assert e == 0 and np.array_equal(s, exp_s)
+    key = wl.bf16_normal((1, R, H, D), 711)
+    for kind in ("paged", "range"):
+        kc = torch.zeros((1, B, T, H, D), dtype=torch.bfloat16, device=dev())
+        vc = torch.zeros_like(kc)
+        e2 = err_word()
+        if kind == "paged":
+            sf = kv.kv_slot_mapping_paged_write(cuda(q), cuda(pos), cuda(table), T, B,
+                                                key.to(dev()), key.to(dev()), kc, vc,
+                                                max_num_tokens=n_max, err=e2)
+        else:
+            sf = kv.kv_slot_mapping_range_write(cuda(q), cuda(pos), cuda(rs), cuda(rl),
+                                                cuda(nr), T, B, key.to(dev()), key.to(dev()),
+                                                kc, vc, max_num_tokens=n_max, err=e2)
+        assert int(e2.item()) == 0, kind
+        assert np.array_equal(sf.cpu().numpy(), exp_s), kind
+        ek = np.zeros((1, B, T, H, D), np.uint16)
+        ev = ek.copy()
+        assert oracle.cache_write(bits(key), bits(key), ek, ev, exp_s[:R], B, T) == 0
+        assert np.array_equal(bits(kc), ek) and np.array_equal(bits(vc), ev), kind
+
+
 def test_many_requests_qsl_in_global_memory():
     rng = np.random.default_rng(7)
     R, T = 9000, 16
