@@ -1011,8 +1011,8 @@ def paged_vs_range(torch, kv, built, steps, reps, flush_buf, stream):
                 "in one CUDA graph; *_fused: kv_slot_mapping_{paged,range}_write, one launch "
                 "in a graph; the four graphs replayed round robin with the L2 flushed before "
                 "each replay, all writing one shared slot buffer.  per_launch_us: each call "
-                "alone, L2 flushed before it (CUDA events tick in 2.05 us steps; the means are "
-                "over all reps)",
+                "alone, L2 flushed before it (the means are over all reps: a single "
+                "latency-bound launch varies by about 1 us)",
     }
 
 
