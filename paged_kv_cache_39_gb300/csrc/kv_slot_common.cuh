@@ -25,9 +25,9 @@ struct SlotArgs {
 };
 
 // Stage query_start_loc in shared memory when it fits.
-// `overlap()` runs once the thread's first staging load is in flight and
-// before the barrier: work that waits on other loads (a position) can then
-// issue its own loads without holding the staging back.
+// `overlap()` runs once the thread's staging loads are in flight and before
+// the barrier: work that waits on other loads (a position) can then issue
+// its own loads without holding the staging back.
 // Up to kStageLoads entries per thread are requested before any is stored,
 // so up to kStageLoads * blockDim entries arrive in one round trip (a
 // 256-request batch has 257: with one load per thread before the store,
@@ -83,8 +83,8 @@ __device__ __forceinline__ int request_of(const int32_t* q, int n, int32_t t) {
 }
 
 // Same, trying request t first: a decode batch gives request t its token t,
-// and two shared-memory reads confirm it where the search takes about nine
-// dependent ones.  Exact whenever query_start_loc is non-decreasing (spans
+// and two reads of q (shared memory when staged) confirm it where the search
+// takes about nine dependent ones.  Exact whenever query_start_loc is non-decreasing (spans
 // are then disjoint); with a malformed one the slots are unspecified anyway.
 __device__ __forceinline__ int request_of_guess(const int32_t* q, int n, int32_t t) {
   if (t < n && q[t] <= t && t < q[t + 1]) return t;
