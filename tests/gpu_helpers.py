@@ -106,7 +106,7 @@ def check_write(key, val, kc, vc, slots_host, L, N, B, T, E, rng):
 # shifted or truncated query_start_loc, untracked tokens, padding tails,
 # negative and out-of-range positions, null and out-of-range table entries.
 def random_slot_case(rng):
-    T = int(rng.choice([1, 4, 16, 32]))
+    T = int(rng.choice([1, 3, 4, 12, 16, 24, 32]))  # non-powers of two take the division paths
     R = int(rng.integers(0, 40))
     lens = rng.integers(0, 70, size=R)
     lens[rng.random(R) < 0.2] = 0

@@ -104,7 +104,7 @@ def test_slot_maps_and_fused_stress(seed):
 def test_gathers_and_copies_stress(seed):
     rng = np.random.default_rng(200000 + seed)
     R = int(rng.integers(1, 300))
-    T = int(rng.choice([1, 4, 8, 16]))
+    T = int(rng.choice([1, 4, 6, 8, 12, 16]))
     stride = int(rng.integers(1, 12))
     B = int(rng.integers(2, 80))
     L = int(rng.integers(1, 3))
@@ -185,7 +185,7 @@ def _prefill_batch(rng):
     q = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64) + shift
     q[-1] = min(q[-1], N)
     n_max = N + int(rng.choice([0, 5, 3000]))
-    T = int(rng.choice([16, 16, 32]))
+    T = int(rng.choice([16, 16, 24, 32]))
     B = 400_000
     pos = np.empty(N, np.int64)
     for r in range(R):
