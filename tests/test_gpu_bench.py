@@ -36,8 +36,9 @@ def test_gpu_arm_line():
     assert d["n_gpus"] == 1 and d["steps"] == STEPS and d["warmup"] == WARMUP
     assert d["scaling"] == "weak" and d["vs_baseline"] is None and d["data"] == "synthetic"
     assert d["value"] > 0 and d["ms_per_step"] > 0
-    # value: the batch's 256 new tokens over the mean step time
-    assert abs(d["value"] - 256 / (d["ms_per_step"] * 1e-3)) <= 1e-3 * d["value"]
+    # value: the batch's 256 new tokens over the mean step time (ms_per_step is
+    # rounded to 10 ns)
+    assert abs(d["value"] - 256 / (d["ms_per_step"] * 1e-3)) <= 2e-3 * d["value"]
     assert d["config"]["workload"] == bench.DECODE_DESC + " [small]"
     assert "flushed" in d["config"]["l2"]
     assert d["gpu_launches"] == STEPS * 3
