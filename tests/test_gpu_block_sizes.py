@@ -131,3 +131,27 @@ def test_large_block_sizes(T, H, D):
         kv.kv_copy_blocks(kc_c, vc_c, cuda(src_b), cuda(dst_b), err=e, bulk=bulk)
         assert int(e.item()) == exp_ce
         assert np.array_equal(bits(kc_c), ck) and np.array_equal(bits(vc_c), cv), bulk
+
+
+@pytest.mark.parametrize("mgr_bs,kern_bs,extra", [(528, 16, 0), (1056, 16, 5), (2048, 16, 0),
+                                                  (528, 48, 2)])
+def test_expand_large_ratios(mgr_bs, kern_bs, extra):
+    """Manager blocks of 528 to 2048 tokens unfolded into 16- or 48-token
+    kernel blocks (k = 11 to 128 kernel entries per manager entry), with null
+    and negative entries and one whose last kernel block overflows int32."""
+    k = mgr_bs // kern_bs
+    rng = np.random.default_rng(16000 + mgr_bs + kern_bs)
+    R, Ms = 9, 7
+    mgr = rng.integers(-2, (1 << 31) // k, size=(R, Ms)).astype(np.int32)
+    mgr[rng.random(mgr.shape) < 0.3] = 0
+    mgr[1, 2] = (1 << 31) // k  # m * k + (k - 1) passes INT32_MAX
+    mgr[2, 0], mgr[4, 6] = -1, -7
+    Ks = Ms * k + extra
+    exp, exp_e = oracle.expand_kernel_blocks(mgr, mgr_bs, kern_bs, Ks)
+    assert exp_e != 0  # the negative and the overflowing entries
+    e = err_word()
+    out = kv.kv_expand_kernel_blocks(cuda(mgr), mgr_bs, kern_bs,
+                                     kernel_table=torch.full((R, Ks), 77, dtype=torch.int32,
+                                                             device=dev()), err=e)
+    assert int(e.item()) == exp_e
+    assert np.array_equal(out.cpu().numpy(), exp)
