@@ -1,8 +1,9 @@
-"""Large block sizes through the whole path: both slot maps, the fused calls,
+"""Large shapes through the whole path: both slot maps, the fused calls,
 the write, the three gathers and both block copies at 128 to 2048 tokens per
 block (528, not a power of two, is a size hybrid attention/state-space models
-give their attention blocks).  Every result is compared with the oracle bit for
-bit."""
+give their attention blocks); expansion ratios of 11 to 128; 80 and 128
+layers; rows of 32 and 40 KiB.  Every result is compared with the oracle bit
+for bit."""
 import numpy as np
 import pytest
 import torch
@@ -155,3 +156,65 @@ def test_expand_large_ratios(mgr_bs, kern_bs, extra):
                                                              device=dev()), err=e)
     assert int(e.item()) == exp_e
     assert np.array_equal(out.cpu().numpy(), exp)
+
+
+@pytest.mark.parametrize("L,H,D", [(80, 1, 8), (128, 2, 16), (2, 64, 256), (3, 20, 1024)])
+def test_many_layers_and_wide_rows(L, H, D):
+    """80 and 128 layers of small rows, and rows of 32 and 40 KiB (64 heads x
+    256, 20 x 1024), through the write, the fused paged call, the gather of
+    the last layer and both block copies (the bulk forms refuse rows past 32
+    KiB, where the vector forms run)."""
+    T = 16
+    B, table, rs, rl, nr, qsl, pos = _case(T, 17000 + L + H + D)
+    N = int(qsl[-1])
+    exp_s, exp_e = oracle.slot_mapping_paged(qsl, pos, table, N, N, T, B)
+    key = wl.bf16_normal((L, N, H, D), 170)
+    val = wl.bf16_normal((L, N, H, D), 171)
+    kc = wl.bf16_normal((L, B, T, H, D), 172)
+    vc = wl.bf16_normal((L, B, T, H, D), 173)
+    ek, ev = bits(kc).copy(), bits(vc).copy()
+    exp_we = oracle.cache_write(bits(key), bits(val), ek, ev, exp_s, B, T)
+    kd, vd = key.to(dev()), val.to(dev())
+    kc_d, vc_d = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    kv.kv_cache_write(kd, vd, kc_d, vc_d, cuda(exp_s), err=e)
+    assert int(e.item()) == exp_we
+    assert np.array_equal(bits(kc_d), ek) and np.array_equal(bits(vc_d), ev)
+    kc_f, vc_f = kc.to(dev()), vc.to(dev())
+    e = err_word()
+    s = kv.kv_slot_mapping_paged_write(cuda(qsl), cuda(pos), cuda(table), T, B, kd, vd, kc_f,
+                                       vc_f, err=e)
+    assert np.array_equal(s.cpu().numpy(), exp_s) and int(e.item()) == exp_e | exp_we
+    assert np.array_equal(bits(kc_f), ek) and np.array_equal(bits(vc_f), ev)
+    del kc_f, vc_f
+
+    R, stride = table.shape
+    g0 = np.array([0, 5, 17], np.int32)
+    g1 = np.array([stride * T, 38, 17 + T], np.int32)
+    out_rows = int((g1 - g0).sum())
+    ko = np.zeros((out_rows, H, D), np.uint16)
+    vo = np.zeros((out_rows, H, D), np.uint16)
+    exp_ge = oracle.cache_gather(ek, ev, L - 1, B, T, table, g0, g1, ko, vo)
+    for bulk in (False, True):
+        e = err_word()
+        args = (kc_d, vc_d, cuda(table), cuda(g0), cuda(g1))
+        if bulk and H * D * 2 > 32768:
+            with pytest.raises(kv.KVError) as ei:
+                kv.kv_cache_gather(*args, layer=L - 1, out_rows=out_rows, err=e, bulk=True)
+            assert ei.value.status == kv.KV_EUNSUPPORTED
+            continue
+        k_out, v_out = kv.kv_cache_gather(*args, layer=L - 1, out_rows=out_rows, err=e,
+                                          bulk=bulk)
+        assert int(e.item()) == exp_ge
+        assert np.array_equal(bits(k_out), ko) and np.array_equal(bits(v_out), vo), bulk
+
+    src_b = np.array([table[0, 1], table[2, 3], 0], np.int32)
+    dst_b = np.array([B - 1, B - 2, B - 3], np.int32)
+    for bulk in (False, True):
+        ck, cv = ek.copy(), ev.copy()
+        exp_ce = oracle.copy_blocks(ck, cv, src_b, dst_b)
+        kc_c, vc_c = kc_d.clone(), vc_d.clone()
+        e = err_word()
+        kv.kv_copy_blocks(kc_c, vc_c, cuda(src_b), cuda(dst_b), err=e, bulk=bulk)
+        assert int(e.item()) == exp_ce
+        assert np.array_equal(bits(kc_c), ck) and np.array_equal(bits(vc_c), cv), bulk
