@@ -84,6 +84,46 @@ MUTANTS = [
     ("cp_local_offset_dropped_stripe", "return b * T + (v / ((int64_t)I * W)) * I + p % I;",
      "return b * T + (v / I) + p % I;"),
     ("expand_divisor_unchecked", "if (mgr_block_size % kernel_block_size != 0) return ORC_EUNSUPPORTED;", ""),
+    ("qsl_order_unchecked", "if (qsl[r] > qsl[r + 1]) e |= ORC_BAD_QSL;", ";"),
+    ("qsl_end_unchecked", "if (qsl[0] < 0 || qsl[R] > N) e |= ORC_BAD_QSL;",
+     "if (qsl[0] < 0) e |= ORC_BAD_QSL;"),
+    ("range_count_unflagged", "if (nr < 0 || nr > range_stride) return ORC_BAD_RANGE;",
+     "if (nr < 0 || nr > range_stride) return 0;"),
+    ("range_negative_len_counted",
+     "        int64_t len = rlen[i] > 0 ? rlen[i] : 0;\n        if (range_cum <= lb",
+     "        int64_t len = rlen[i];\n        if (range_cum <= lb"),
+    ("range_null_block_written", "            if (b == ORC_NULL_BLOCK) return ORC_PAD_SLOT;\n", ""),
+    ("range_malformed_row_resolved", "    if (nr < 0 || nr > range_stride) return ORC_PAD_SLOT;\n",
+     "    if (nr < 0) return ORC_PAD_SLOT;\n    if (nr > range_stride) nr = range_stride;\n"),
+    ("paged_negative_position_unflagged",
+     "if (p < 0) { *err |= ORC_BAD_POSITION; return ORC_PAD_SLOT; }\n    int64_t lb = p / T;\n"
+     "    if (lb >= stride)",
+     "if (p < 0) { return ORC_PAD_SLOT; }\n    int64_t lb = p / T;\n    if (lb >= stride)"),
+    ("write_bad_slot_unflagged", "if (b >= B) { *err |= ORC_BAD_SLOT; return -1; }",
+     "if (b >= B) { return -1; }"),
+    ("write_v_from_key", "                v_cache[n * E + x] = value[src + x];",
+     "                v_cache[n * E + x] = key[src + x];"),
+    ("gather_past_row_unflagged",
+     "if (lb >= table_stride) { e |= ORC_BAD_POSITION; src_rows[o] = -1; continue; }",
+     "if (lb >= table_stride) { src_rows[o] = -1; continue; }"),
+    ("gather_bad_span_unflagged",
+     "if (s0 < 0 || s1 < s0) { e |= ORC_BAD_POSITION; continue; }\n        const int32_t* row = block_table",
+     "if (s0 < 0 || s1 < s0) { continue; }\n        const int32_t* row = block_table"),
+    ("gather_out_of_space_unflagged",
+     "if (o >= out_rows) { e |= ORC_OUT_OF_SPACE; continue; }\n            int64_t lb = p / block_size;",
+     "if (o >= out_rows) { continue; }\n            int64_t lb = p / block_size;"),
+    ("gather_range_bad_block_unflagged", "if (b < 0 || b >= num_blocks) e |= ORC_BAD_BLOCK;",
+     "if (b < 0 || b >= num_blocks) (void)0;"),
+    ("copy_src_null_allowed", "if (sb <= ORC_NULL_BLOCK || sb >= num_blocks)",
+     "if (sb < ORC_NULL_BLOCK || sb >= num_blocks)"),
+    ("copy_first_layer_only",
+     "for (int32_t l = 0; l < num_layers; ++l)\n            for (int32_t t = 0; t < block_size; ++t) {",
+     "for (int32_t l = 0; l < 1; ++l)\n            for (int32_t t = 0; t < block_size; ++t) {"),
+    ("expand_overflow_unchecked", "if (m < 0 || m * k + (k - 1) > INT32_MAX)", "if (m < 0)"),
+    ("table_from_ranges_zero_len_ok", "if (len <= 0) { e |= ORC_BAD_RANGE; continue; }",
+     "if (len < 0) { e |= ORC_BAD_RANGE; continue; }"),
+    ("table_from_ranges_cut_unflagged", "if (lb >= table_stride) { e |= ORC_OUT_OF_SPACE; break; }",
+     "if (lb >= table_stride) { break; }"),
 ]
 
 

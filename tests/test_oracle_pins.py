@@ -219,6 +219,24 @@ def test_table_from_ranges_matches_concatenation(seed):
     assert err == exp_err
 
 
+def test_table_from_ranges_zero_length_and_cut_rows():
+    """A range of length 0 covers nothing and marks its row malformed; ranges
+    reaching past the table row are cut at its end.  Each case alone, so each
+    error bit is pinned on its own."""
+    rs = np.array([[5, 20, 9]], np.int32)
+    rl = np.array([[3, 0, 2]], np.int32)
+    table, err = oracle.table_from_ranges(rs, rl, [3], 8, with_error=True)
+    assert table.tolist() == [[5, 6, 7, 9, 10, 0, 0, 0]]
+    assert err == BITS["BAD_RANGE"]
+    rs = np.array([[1, 30]], np.int32)
+    rl = np.array([[4, 6]], np.int32)
+    table, err = oracle.table_from_ranges(rs, rl, [2], 8, with_error=True)
+    assert table.tolist() == [[1, 2, 3, 4, 30, 31, 32, 33]]
+    assert err == BITS["OUT_OF_SPACE"]
+    table, err = oracle.table_from_ranges(rs, rl, [2], 10, with_error=True)
+    assert table.tolist() == [[1, 2, 3, 4, 30, 31, 32, 33, 34, 35]] and err == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode", "mixed"])
 def test_range_equals_paged_on_expanded_table(name):
     """Range and table strategies give identical slots for the same layout."""
