@@ -48,7 +48,11 @@ def test_gpu_arm_line():
     assert roof["kernel"] in {"slot_mapping_paged_kernel", "slot_mapping_range_kernel",
                               "cache_write_kernel"}
     assert roof["achieved"] > 0 and roof["peak"] > 0
-    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) <= 1e-3 * roof["frac"] + 1e-6
+    # achieved = algorithmic bytes per launch / mean launch time (both printed
+    # rounded: achieved to 0.1 GB/s, the time to 10 ns), frac = achieved / peak
+    gbs = roof["alg_bytes_per_launch"] / (roof["avg_launch_us"] * 1e-6) / 1e9
+    assert abs(roof["achieved"] - gbs) <= 0.05 + 2e-3 * gbs
+    assert abs(roof["frac"] - gbs / roof["peak"]) <= 2e-3 * gbs / roof["peak"] + 1e-6
     peaks = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks):
         assert roof["peak_kind"].startswith("measured")
