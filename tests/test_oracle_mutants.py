@@ -8,6 +8,7 @@ Mistakes are planted on the CPU, in the oracle only.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -127,17 +128,39 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,orig,planted", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(name, orig, planted, tmp_path):
-    src = open(SOURCE).read()
-    assert src.count(orig) == 1, f"mutation anchor for {name} must occur exactly once"
-    mutant = tmp_path / "kv_oracle_mutant.c"
-    mutant.write_text(src.replace(orig, planted))
+def _run_mutant(src, base, mutant):
+    """Build one planted copy of the oracle and run the pin suite against it;
+    returns the suite's exit code and the end of its output."""
+    name, orig, planted = mutant
+    if src.count(orig) != 1:
+        return None, f"mutation anchor for {name} must occur exactly once"
+    d = base / name
+    d.mkdir()
+    path = d / "kv_oracle_mutant.c"
+    path.write_text(src.replace(orig, planted))
     lib = build_oracle(extra_flags=["-Wno-unused-parameter", "-Wno-unused-variable",
                                     "-Wno-unused-but-set-variable"],
-                       source=str(mutant), out=str(tmp_path / "libmutant.so"))
+                       source=str(path), out=str(d / "libmutant.so"))
     env = dict(os.environ, KV_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
-    assert r.returncode != 0, f"planted mistake {name} went unnoticed:\n{r.stdout[-2000:]}"
+    return r.returncode, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_runs(tmp_path_factory):
+    """Every planted copy built and pinned, several at a time (each run is its
+    own compiler and interpreter process)."""
+    src = open(SOURCE).read()
+    base = tmp_path_factory.mktemp("mutants")
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+        runs = list(ex.map(lambda m: _run_mutant(src, base, m), MUTANTS))
+    return {m[0]: r for m, r in zip(MUTANTS, runs)}
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, mutant_runs):
+    rc, out = mutant_runs[name]
+    assert rc is not None, out
+    assert rc != 0, f"planted mistake {name} went unnoticed:\n{out}"
