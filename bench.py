@@ -83,7 +83,7 @@ _REASONS = [(0x1, "gpu_idle"), (0x2, "applications_clocks_setting"), (0x4, "sw_p
 class ClockSampler:
     """Samples the SM clock and clock-event reasons through NVML (read only)."""
 
-    def __init__(self, period_s: float = 0.005):
+    def __init__(self, period_s: float = 0.002):
         self.period = period_s
         self.samples = []
         self.reasons = 0
@@ -121,18 +121,23 @@ class ClockSampler:
         except Exception:
             return None
 
-    def _loop(self):
+    def _sample(self):
         clk = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
-        while not self._stop.is_set():
-            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
-                self.samples.append(int(clk.value))
-            if self._reasons_fn(self._h, ctypes.byref(rs)) == 0:
-                self.reasons |= int(rs.value)
-            time.sleep(self.period)
+        if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(int(clk.value))
+        if self._reasons_fn(self._h, ctypes.byref(rs)) == 0:
+            self.reasons |= int(rs.value)
+
+    def _loop(self):
+        while not self._stop.wait(self.period):
+            self._sample()
 
     def __enter__(self):
+        # a sample as the region starts, every period inside it, one as it ends:
+        # a short region (20 steps take a few ms) still gets several
         if self._nvml is not None:
+            self._sample()
             self._thread = threading.Thread(target=self._loop, daemon=True)
             self._thread.start()
         return self
@@ -141,6 +146,7 @@ class ClockSampler:
         self._stop.set()
         if self._thread is not None:
             self._thread.join()
+            self._sample()
 
     def summary(self):
         if self._nvml is None:
