@@ -1127,9 +1127,36 @@ def decode_step_with_gather(torch, built, steps, flush_buf, stream, peak, args):
 # end to end through the public API with host buffers
 # --------------------------------------------------------------------------
 
-def e2e_step(torch, kv, built, steps, flush_buf, stream):
+def device_alias(torch, host, dev):
+    """A CUDA int32 tensor over the same bytes as the pinned host tensor
+    `host` (page-locked memory is mapped into the device's address space, at
+    the same address), or None when the driver reports no such mapping."""
+    try:
+        cudart = ctypes.CDLL("libcudart.so.13")
+        attr = (ctypes.c_char * 256)()
+        if cudart.cudaPointerGetAttributes(attr, ctypes.c_void_p(host.data_ptr())) != 0:
+            return None
+        kind = ctypes.c_int.from_buffer(attr, 0).value
+        dptr = ctypes.c_void_p.from_buffer(attr, 8).value
+        if kind != 1 or dptr != host.data_ptr():  # 1: page-locked host memory
+            return None
+
+        class _Iface:
+            __cuda_array_interface__ = {"shape": (host.numel() * host.element_size() // 4,),
+                                        "typestr": "<i4", "data": (host.data_ptr(), False),
+                                        "version": 3, "strides": None}
+        alias = torch.as_tensor(_Iface(), device=dev)
+    except Exception:
+        return None
+    return alias if alias.data_ptr() == host.data_ptr() else None
+
+
+def e2e_step(torch, kv, built, steps, flush_buf, stream, upload="sm"):
     """The headline step through the public API from host memory: every step
-    copies its inputs from pinned host memory (packed, one copy), runs the
+    copies its inputs from pinned host memory (packed, one copy: an
+    elementwise kernel reading the pinned buffer through its device mapping,
+    13.5-13.6 against 13.8-14.3 us per step by the copy engine, which is used
+    where the driver reports no mapping or with upload="ce"), runs the
     three prepared calls (paged map -> write, the range map on a second
     branch, as in the device-resident step), and copies both slot mappings and
     the error word back to pinned host memory, where the host checks them.
@@ -1165,6 +1192,7 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
         src = host_src[n]
         src = torch.from_numpy(np.ascontiguousarray(src)) if isinstance(src, np.ndarray) else src
         h_stage[offs[n]:offs[n] + nbytes].copy_(src.contiguous().view(-1).view(torch.uint8))
+    h_alias = device_alias(torch, h_stage, dev) if upload == "sm" else None
     T, B, n_max = w.block_size, w.num_blocks, w.max_num_tokens
     n_slot = k["slot_p"].numel()
     out_bytes = 256 + 2 * n_slot * 8  # error word (256-byte slot), both slot mappings
@@ -1180,6 +1208,7 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
             # inputs and the error word, the read-back the error word and slots
             buf = torch.zeros(total + out_bytes, dtype=torch.uint8, device=dev)
             self.d_in, self.d_out = buf[:total + 256], buf[total:]
+            self.d_in32 = self.d_in.view(torch.int32)
             d = {n: buf[offs[n]:offs[n] + k[n].numel() * k[n].element_size()]
                  .view(k[n].dtype).view(k[n].shape) for n in names}
             self.h_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
@@ -1204,7 +1233,11 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
             self.done = torch.cuda.Event()
 
         def upload(self):
-            self.d_in.copy_(h_stage, non_blocking=True)
+            if h_alias is not None:
+                # the SMs read the pinned inputs over the chip-to-chip link
+                torch.bitwise_or(h_alias, 0, out=self.d_in32)
+            else:
+                self.d_in.copy_(h_stage, non_blocking=True)
 
         def compute(self):
             paged, rng, write = self.calls
@@ -1296,6 +1329,8 @@ def e2e_step(torch, kv, built, steps, flush_buf, stream):
     del graphs, serial, sets
     return {"value": round(built.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": int(total + 256), "d2h_bytes_per_step": int(out_bytes),
+            "upload": ("an elementwise kernel reading the pinned buffer" if h_alias is not None
+                       else "the copy engine"),
             "ms_per_step": round(ms, 4), "steps": n_steps,
             "sync_ms_per_step": round(statistics.median(times) * 1e3, 4),
             "note": "wall time over all steps: each step copies one step's packed inputs "
